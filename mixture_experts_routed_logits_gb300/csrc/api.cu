@@ -1,0 +1,469 @@
+// api.cu -- host side of the C ABI declared in include/ts_moe.h: argument validation, the
+// workspace layout and the launch sequence.  Every check runs before anything is launched;
+// a request the kernels cannot serve is refused with a message, never degraded (the pages'
+// convention: the Gemma-4 batched routed prefill returns Unsupported rather than quietly
+// looping the per-token kernels).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/ts_moe.h"
+#include "internal.h"
+
+using namespace tsmoe;
+
+namespace {
+
+thread_local std::string g_err;
+thread_local cudaEvent_t g_phase_ev[8];
+thread_local int g_phase_n = 0;
+
+// records phase event i (if registered) on the stream; capture-safe
+cudaError_t phase_mark(int i, cudaStream_t st) {
+    if (i >= g_phase_n || !g_phase_ev[i]) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(g_phase_ev[i], st, cudaEventRecordExternal);
+    return cudaEventRecord(g_phase_ev[i], st);
+}
+
+ts_status fail(ts_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+ts_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(TS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+inline bool aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+int num_sms_current() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+inline size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+size_t matrix_bytes(int fmt, int R, int K) {
+    if (fmt == FMT_F16 || fmt == FMT_BF16) return static_cast<size_t>(R) * K * 2;
+    return static_cast<size_t>(R / kRowTile) * (K / kBlockK) * packed_block_bytes(fmt);
+}
+
+ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
+    if (!ex) return fail(TS_ERR_INVALID_ARG, "%s: descriptor is NULL", what);
+    if (ex->fmt < 0 || ex->fmt > 3) return fail(TS_ERR_INVALID_ARG, "%s: bad weight format %d", what, ex->fmt);
+    if (ex->act < 0 || ex->act > 2) return fail(TS_ERR_INVALID_ARG, "%s: bad activation %d", what, ex->act);
+    if (ex->E < 1 || ex->E > kMaxExperts)
+        return fail(TS_ERR_UNSUPPORTED, "%s: E=%d outside 1..%d", what, ex->E, kMaxExperts);
+    if (ex->H <= 0 || ex->I <= 0 || ex->H % kBlockK || ex->I % kBlockK)
+        return fail(TS_ERR_UNSUPPORTED, "%s: H=%d and I=%d must be positive multiples of 32", what,
+                    ex->H, ex->I);
+    if (!ex->gate || !ex->up || !ex->down)
+        return fail(TS_ERR_INVALID_ARG, "%s: gate/up/down weight pointer is NULL", what);
+    if (!aligned(ex->gate, 16) || !aligned(ex->up, 16) || !aligned(ex->down, 16))
+        return fail(TS_ERR_INVALID_ARG, "%s: weight pointers must be 16-byte aligned", what);
+    if (!aligned(ex->gate_b, 2) || !aligned(ex->up_b, 2) || !aligned(ex->down_b, 2))
+        return fail(TS_ERR_INVALID_ARG, "%s: bias pointers must be 2-byte aligned", what);
+    if (ex->fmt == FMT_BF16 && adt != TS_DT_BF16)
+        return fail(TS_ERR_UNSUPPORTED,
+                    "%s: bf16 weights need bf16 activations (f16 activations would be rounded)", what);
+    return TS_OK;
+}
+
+struct WsLayout {
+    size_t status, off, perm, inv, h, e, hs, s, xs, total;
+};
+
+WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts* sh) {
+    WsLayout L{};
+    size_t a = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = a;
+        a = round_up(a + bytes, 256);
+        return o;
+    };
+    const size_t Tk = static_cast<size_t>(T) * k;
+    L.status = take(256);
+    L.off = take(static_cast<size_t>(ex->E + 1) * 4);
+    L.perm = take(Tk * 4);
+    L.inv = take(Tk * 4);
+    L.h = take(Tk * ex->I * 2);
+    L.e = take(Tk * ex->H * 4);
+    if (sh) {
+        L.hs = take(static_cast<size_t>(T) * sh->I * 2);
+        L.s = take(static_cast<size_t>(T) * ex->H * 4);
+    }
+    L.xs = take(Tk * ex->H * 2);   // activations in route-list order (tensor-core path)
+    L.total = a;
+    return L;
+}
+
+ts_status launch_gemv_checked(const GemvArgs& a, cudaStream_t st, const char* what) {
+    const int sms = num_sms_current();
+    if (sms <= 0) return fail(TS_ERR_CUDA, "%s: no CUDA device", what);
+    cudaError_t e = launch_gemv(a, sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return TS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ts_last_error(void) { return g_err.c_str(); }
+
+const char* ts_moe_version(void) { return "0.1.0"; }
+
+size_t ts_moe_packed_bytes(int32_t fmt, int32_t nmat, int32_t R, int32_t K) {
+    if ((fmt != TS_W_MXFP4 && fmt != TS_W_INT4_AFFINE) || nmat < 1 || R <= 0 || K <= 0 ||
+        R % kRowTile || K % kBlockK)
+        return 0;
+    return static_cast<size_t>(nmat) * matrix_bytes(fmt, R, K);
+}
+
+ts_status ts_moe_pack(int32_t fmt, int32_t nmat, int32_t R, int32_t K, const void* codes,
+                      const void* scales, void* packed, size_t packed_bytes, void* stream) {
+    g_err.clear();
+    const size_t need = ts_moe_packed_bytes(fmt, nmat, R, K);
+    if (need == 0)
+        return fail(TS_ERR_INVALID_ARG,
+                    "ts_moe_pack: fmt must be MXFP4 or INT4_AFFINE, R %% 16 == 0, K %% 32 == 0 "
+                    "(fmt=%d nmat=%d R=%d K=%d)", fmt, nmat, R, K);
+    if (!codes || !scales || !packed) return fail(TS_ERR_INVALID_ARG, "ts_moe_pack: NULL pointer");
+    if (!aligned(packed, 16)) return fail(TS_ERR_INVALID_ARG, "ts_moe_pack: packed must be 16-byte aligned");
+    if (packed_bytes < need)
+        return fail(TS_ERR_INVALID_ARG, "ts_moe_pack: packed_bytes %zu < %zu", packed_bytes, need);
+    cudaError_t e = launch_pack(fmt, nmat, R, K, static_cast<const uint8_t*>(codes),
+                                static_cast<const uint8_t*>(scales), static_cast<uint8_t*>(packed),
+                                static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_pack");
+    return TS_OK;
+}
+
+static ts_status route_common(RouteArgs& a, cudaStream_t st, const char* what) {
+    if (a.T < 0) return fail(TS_ERR_INVALID_ARG, "%s: T=%d < 0", what, a.T);
+    if (a.E < 1 || a.E > kMaxExperts)
+        return fail(TS_ERR_UNSUPPORTED, "%s: E=%d outside 1..%d", what, a.E, kMaxExperts);
+    if (a.k < 1 || a.k > a.E) return fail(TS_ERR_INVALID_ARG, "%s: k=%d outside 1..E=%d", what, a.k, a.E);
+    if (a.mode < 0 || a.mode > 2) return fail(TS_ERR_INVALID_ARG, "%s: bad mode %d", what, a.mode);
+    if (a.mode == MODE_SOFTMAX_K_SCALED && !a.scale)
+        return fail(TS_ERR_INVALID_ARG, "%s: SOFTMAX_K_SCALED needs per_expert_scale", what);
+    if (a.T == 0) return TS_OK;
+    if (!a.idx || !a.w) return fail(TS_ERR_INVALID_ARG, "%s: idx/w output is NULL", what);
+    cudaError_t e = launch_router(a, st);
+    if (e == cudaSuccess) e = phase_mark(6, st);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return TS_OK;
+}
+
+ts_status ts_moe_route(const float* logits, const float* router_bias,
+                       const float* per_expert_scale, int32_t T, int32_t E, int32_t k,
+                       int32_t mode, int32_t* idx, float* w, void* stream) {
+    g_err.clear();
+    RouteArgs a{};
+    a.logits_in = logits;
+    a.bias = router_bias;
+    a.scale = per_expert_scale;
+    a.idx = idx;
+    a.w = w;
+    a.T = T;
+    a.E = E;
+    a.k = k;
+    a.mode = mode;
+    if (T > 0 && !logits) return fail(TS_ERR_INVALID_ARG, "ts_moe_route: logits is NULL");
+    return route_common(a, static_cast<cudaStream_t>(stream), "ts_moe_route");
+}
+
+ts_status ts_moe_router_route(const void* x, int32_t adt, int32_t T, int32_t H, const void* W_r,
+                              int32_t E, int32_t rmsnorm, float eps, const float* router_bias,
+                              const float* per_expert_scale, int32_t k, int32_t mode,
+                              void* xn_out, float* logits_out, int32_t* idx, float* w,
+                              void* stream) {
+    g_err.clear();
+    const char* what = "ts_moe_router_route";
+    if (adt != TS_DT_F16 && adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, adt);
+    if (H <= 0 || H % kBlockK) return fail(TS_ERR_UNSUPPORTED, "%s: H=%d must be a positive multiple of 32", what, H);
+    if (H > 12288) return fail(TS_ERR_UNSUPPORTED, "%s: H=%d above 12288", what, H);
+    if (rmsnorm != 0 && rmsnorm != 1) return fail(TS_ERR_INVALID_ARG, "%s: rmsnorm must be 0 or 1", what);
+    if (T > 0 && (!x || !W_r)) return fail(TS_ERR_INVALID_ARG, "%s: x or W_r is NULL", what);
+    if (T > 0 && rmsnorm && !xn_out) return fail(TS_ERR_INVALID_ARG, "%s: rmsnorm needs xn_out", what);
+    if (!(eps >= 0.0f)) return fail(TS_ERR_INVALID_ARG, "%s: eps must be >= 0", what);
+    RouteArgs a{};
+    a.x = x;
+    a.Wr = W_r;
+    a.bias = router_bias;
+    a.scale = per_expert_scale;
+    a.xn_out = xn_out;
+    a.logits_out = logits_out;
+    a.idx = idx;
+    a.w = w;
+    a.T = T;
+    a.H = H;
+    a.E = E;
+    a.k = k;
+    a.mode = mode;
+    a.adt = adt;
+    a.rmsnorm = rmsnorm;
+    a.eps = eps;
+    return route_common(a, static_cast<cudaStream_t>(stream), what);
+}
+
+ts_status ts_moe_build_routes(const int32_t* idx, int32_t T, int32_t E, int32_t k, int32_t* off,
+                              int32_t* perm, int32_t* inv, void* stream) {
+    g_err.clear();
+    const char* what = "ts_moe_build_routes";
+    if (T < 0 || k < 1 || E < 1) return fail(TS_ERR_INVALID_ARG, "%s: bad T/E/k", what);
+    if (E > kMaxExperts) return fail(TS_ERR_UNSUPPORTED, "%s: E=%d above %d", what, E, kMaxExperts);
+    if (static_cast<long long>(T) * k > (1ll << 24))
+        return fail(TS_ERR_UNSUPPORTED, "%s: T*k above 2^24", what);
+    if (!off || (T > 0 && (!idx || !perm || !inv))) return fail(TS_ERR_INVALID_ARG, "%s: NULL pointer", what);
+    cudaError_t e = launch_build_routes(idx, T, E, k, off, perm, inv, nullptr,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return TS_OK;
+}
+
+size_t ts_moe_workspace_size(int32_t T, int32_t k, const ts_moe_experts* ex,
+                             const ts_moe_experts* shared) {
+    if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->H <= 0 || ex->I <= 0) return 0;
+    if (shared && (shared->I <= 0)) return 0;
+    return ws_layout(T, k, ex, shared).total;
+}
+
+ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
+                              const int32_t* idx, const float* w, int32_t k,
+                              const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
+                              size_t ws_bytes, int32_t path, void* stream) {
+    g_err.clear();
+    const char* what = "ts_moe_forward";
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (adt != TS_DT_F16 && adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, adt);
+    if (T < 0) return fail(TS_ERR_INVALID_ARG, "%s: T=%d < 0", what, T);
+    ts_status s = check_experts(ex, "ts_moe_forward: experts", adt);
+    if (s != TS_OK) return s;
+    if (k < 1 || k > ex->E) return fail(TS_ERR_INVALID_ARG, "%s: k=%d outside 1..E=%d", what, k, ex->E);
+    if (shared) {
+        s = check_experts(shared, "ts_moe_forward: shared expert", adt);
+        if (s != TS_OK) return s;
+        if (shared->E != 1 || shared->H != ex->H)
+            return fail(TS_ERR_INVALID_ARG, "%s: shared expert needs E=1 and H=%d", what, ex->H);
+    }
+    if (path < TS_PATH_AUTO || path > TS_PATH_GEMM) return fail(TS_ERR_INVALID_ARG, "%s: bad path %d", what, path);
+    if (static_cast<long long>(T) * k > (1ll << 24)) return fail(TS_ERR_UNSUPPORTED, "%s: T*k above 2^24", what);
+    if (T == 0) return TS_OK;
+    if (!x || !idx || !w || !y) return fail(TS_ERR_INVALID_ARG, "%s: x/idx/w/y is NULL", what);
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(y_f32, 16))
+        return fail(TS_ERR_INVALID_ARG, "%s: x, y and y_f32 must be 16-byte aligned", what);
+    const WsLayout L = ws_layout(T, k, ex, shared);
+    if (!ws) return fail(TS_ERR_WORKSPACE, "%s: workspace is NULL", what);
+    if (!aligned(ws, 256)) return fail(TS_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", what);
+    if (ws_bytes < L.total) return fail(TS_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu", what, ws_bytes, L.total);
+    const bool gemm_fmt = (ex->fmt == FMT_BF16 && adt == TS_DT_BF16) ||
+                          (ex->fmt == FMT_F16 && adt == TS_DT_F16);
+    const bool gemm_shape = ex->H % 64 == 0 && ex->I % 64 == 0;
+    if (path == TS_PATH_GEMM && !(gemm_fmt && gemm_shape))
+        return fail(TS_ERR_UNSUPPORTED,
+                    "%s: the tensor-core path serves 16-bit weights of the activation type with "
+                    "H %% 64 == 0 and I %% 64 == 0 (fmt=%d adt=%d H=%d I=%d)", what, ex->fmt, adt,
+                    ex->H, ex->I);
+    const bool use_gemm = path == TS_PATH_GEMM || (path == TS_PATH_AUTO && T > 8 && gemm_fmt && gemm_shape);
+
+    unsigned char* W = static_cast<unsigned char*>(ws);
+    int* status = reinterpret_cast<int*>(W + L.status);
+    int32_t* off = reinterpret_cast<int32_t*>(W + L.off);
+    int32_t* perm = reinterpret_cast<int32_t*>(W + L.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(W + L.inv);
+
+    cudaError_t e = launch_build_routes(idx, T, ex->E, k, off, perm, inv, status, st);
+    if (e == cudaSuccess) e = phase_mark(0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: route list");
+
+    if (use_gemm) {
+        const int sms = num_sms_current();
+        if (sms <= 0) return fail(TS_ERR_CUDA, "%s: no CUDA device", what);
+        uint16_t* xs = reinterpret_cast<uint16_t*>(W + L.xs);
+        e = launch_gather_rows(static_cast<const uint16_t*>(x), perm, k, ex->H, T * k, xs, st);
+        if (e == cudaSuccess) e = phase_mark(0, st);
+        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: gather");
+        GemmArgs G{};
+        G.phase = 0;
+        G.ab_bf16 = adt == TS_DT_BF16 ? 1 : 0;
+        G.act = ex->act;
+        G.limit = ex->swiglu_limit;
+        G.alpha = ex->swiglu_alpha;
+        G.adt = adt;
+        G.w0 = ex->gate;
+        G.w1 = ex->up;
+        G.b0 = static_cast<const uint16_t*>(ex->gate_b);
+        G.b1 = static_cast<const uint16_t*>(ex->up_b);
+        G.R = ex->I;
+        G.K = ex->H;
+        G.E = ex->E;
+        G.act_in = xs;
+        G.rows_in = T * k;
+        G.out = W + L.h;
+        G.off = off;
+        G.perm = perm;
+        G.status = status;
+        e = launch_tc_gemm(G, sms, st);
+        if (e == cudaSuccess) e = phase_mark(1, st);
+        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: tensor-core phase 1");
+        G.phase = 1;
+        G.w0 = ex->down;
+        G.w1 = nullptr;
+        G.b0 = static_cast<const uint16_t*>(ex->down_b);
+        G.b1 = nullptr;
+        G.R = ex->H;
+        G.K = ex->I;
+        G.act_in = W + L.h;
+        G.out = W + L.e;
+        e = launch_tc_gemm(G, sms, st);
+        if (e == cudaSuccess) e = phase_mark(3, st);
+        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: tensor-core phase 2");
+    }
+
+    GemvArgs g{};
+    g.act = ex->act;
+    g.limit = ex->swiglu_limit;
+    g.alpha = ex->swiglu_alpha;
+    g.adt = adt;
+    g.T = T;
+    g.k = k;
+    g.E = ex->E;
+    g.status = status;
+    // phase 1: gate/up + activation -> h (16-bit, by route id)
+    g.fmt = ex->fmt;
+    g.phase = 0;
+    g.w0 = static_cast<const uint8_t*>(ex->gate);
+    g.w1 = static_cast<const uint8_t*>(ex->up);
+    g.b0 = static_cast<const uint16_t*>(ex->gate_b);
+    g.b1 = static_cast<const uint16_t*>(ex->up_b);
+    g.R = ex->I;
+    g.K = ex->H;
+    g.mat_bytes = matrix_bytes(ex->fmt, ex->I, ex->H);
+    g.in = static_cast<const uint16_t*>(x);
+    g.out = W + L.h;
+    g.off = off;
+    g.perm = perm;
+    g.dense = 0;
+    if (!use_gemm) {
+        if ((s = launch_gemv_checked(g, st, "ts_moe_forward: expert phase 1")) != TS_OK) return s;
+        if ((e = phase_mark(1, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
+    }
+    GemvArgs gs = g;
+    if (shared) {
+        gs.fmt = shared->fmt;
+        gs.act = shared->act;
+        gs.limit = shared->swiglu_limit;
+        gs.alpha = shared->swiglu_alpha;
+        gs.E = 1;
+        gs.w0 = static_cast<const uint8_t*>(shared->gate);
+        gs.w1 = static_cast<const uint8_t*>(shared->up);
+        gs.b0 = static_cast<const uint16_t*>(shared->gate_b);
+        gs.b1 = static_cast<const uint16_t*>(shared->up_b);
+        gs.R = shared->I;
+        gs.K = shared->H;
+        gs.mat_bytes = matrix_bytes(shared->fmt, shared->I, shared->H);
+        gs.out = W + L.hs;
+        gs.off = nullptr;
+        gs.perm = nullptr;
+        gs.dense = 1;
+        gs.k = 1;
+        if ((s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 1")) != TS_OK) return s;
+        if ((e = phase_mark(2, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
+    }
+    // phase 2: down projection -> e (f32, by route id)
+    g.phase = 1;
+    g.w0 = static_cast<const uint8_t*>(ex->down);
+    g.w1 = nullptr;
+    g.b0 = static_cast<const uint16_t*>(ex->down_b);
+    g.b1 = nullptr;
+    g.R = ex->H;
+    g.K = ex->I;
+    g.mat_bytes = matrix_bytes(ex->fmt, ex->H, ex->I);
+    g.in = reinterpret_cast<const uint16_t*>(W + L.h);
+    g.out = W + L.e;
+    if (!use_gemm) {
+        if ((s = launch_gemv_checked(g, st, "ts_moe_forward: expert phase 2")) != TS_OK) return s;
+        if ((e = phase_mark(3, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
+    }
+    if (shared) {
+        gs.phase = 1;
+        gs.w0 = static_cast<const uint8_t*>(shared->down);
+        gs.w1 = nullptr;
+        gs.b0 = static_cast<const uint16_t*>(shared->down_b);
+        gs.b1 = nullptr;
+        gs.R = shared->H;
+        gs.K = shared->I;
+        gs.mat_bytes = matrix_bytes(shared->fmt, shared->H, shared->I);
+        gs.in = reinterpret_cast<const uint16_t*>(W + L.hs);
+        gs.out = W + L.s;
+        if ((s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 2")) != TS_OK) return s;
+        if ((e = phase_mark(4, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
+    }
+    CombineArgs c{};
+    c.e = reinterpret_cast<const float*>(W + L.e);
+    c.w = w;
+    c.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
+    c.y = y;
+    c.y_f32 = y_f32;
+    c.T = T;
+    c.H = ex->H;
+    c.k = k;
+    c.adt = adt;
+    e = launch_combine(c, st);
+    if (e == cudaSuccess) e = phase_mark(5, st);
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: combine");
+    return TS_OK;
+}
+
+ts_status ts_moe_forward(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
+                         const int32_t* idx, const float* w, int32_t k,
+                         const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
+                         size_t ws_bytes, void* stream) {
+    return ts_moe_forward_path(x, adt, T, ex, idx, w, k, shared, y, y_f32, ws, ws_bytes,
+                               TS_PATH_AUTO, stream);
+}
+
+ts_status ts_moe_set_phase_events(void* const* events, int32_t n) {
+    g_err.clear();
+    if (n < 0 || n > 8) return fail(TS_ERR_INVALID_ARG, "ts_moe_set_phase_events: n=%d outside 0..8", n);
+    if (!events) n = 0;
+    for (int i = 0; i < 8; ++i) g_phase_ev[i] = (i < n) ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+    g_phase_n = n;
+    return TS_OK;
+}
+
+ts_status ts_moe_device_status(void* ws, int32_t* code, void* stream) {
+    g_err.clear();
+    if (!ws || !code) return fail(TS_ERR_INVALID_ARG, "ts_moe_device_status: NULL pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_device_status");
+    *code = v;
+    return TS_OK;
+}
+
+}  // extern "C"

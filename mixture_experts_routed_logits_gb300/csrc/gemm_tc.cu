@@ -1,0 +1,441 @@
+// gemm_tc.cu -- steps 4-5 of the routed-expert layer for many tokens (prefill): the per-expert
+// gated FFN as a grouped GEMM on the 5th-generation tensor cores (tcgen05, accumulators in
+// TMEM, operands staged by TMA).
+//
+// Source pages (docs.rs, turbospark-runtime 0.3.0):
+//   Gemma-4 batched routed prefill (src/families/gemma4/moe_batch.rs): one route list for the
+//     whole micro-batch, encode_moe_prefill_phase1 (gate/up + activation for every route) and
+//     encode_moe_prefill_phase2_fused (down projection + combine), "bit-exact against M
+//     sequential decode-pair calls".
+//   gpt-oss routed-expert pass (src/families/gptoss/moe.rs): clamped SwiGLU and per-expert
+//     biases inside the expert kernels.
+//
+// Design (GB300, one CTA per SM, persistent):
+//   * Work item = (expert, block of weight rows, tile of <= 256 routes of that expert).  The
+//     routes of an expert are contiguous in the expert-sorted route list, so the activation
+//     tile is a plain 2-D TMA box of the sorted activations.
+//   * Swap-AB: the weights are the MMA's M side (128 rows per accumulator), the routes its N
+//     side (16..256, a multiple of 16, sized to the tile's real route count), so small experts
+//     waste no tensor time on padding.
+//   * Phase 1: two accumulators per item, gate and up of the same 128 rows, 2 x N TMEM columns;
+//     epilogue adds the biases, applies the activation, rounds h to 16 bits and stores it in
+//     route-list order.  Phase 2: two accumulators cover 256 rows of the down projection;
+//     epilogue adds the bias and stores f32 expert outputs by route id for the combine.
+//   * Warp roles: warp 0 = TMA producer (3-stage ring of 64 KB), warp 1 = MMA issuer (one
+//     thread, tcgen05.mma kind::f16, 128B-swizzled K-major smem descriptors), warps 2-5 =
+//     epilogue (tcgen05.ld of their TMEM lane quarter).  Every mbarrier wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace tsmoe {
+
+namespace {
+
+constexpr int kBM = 128;                         // weight rows per accumulator
+constexpr int kBN = 256;                         // max routes per tile
+constexpr int kBK = 64;                          // K elements per stage (128 bytes of 16-bit)
+constexpr int kStages = 3;
+constexpr int kATile = kBM * kBK * 2;            // 16 KB
+constexpr int kBBox = 64 * kBK * 2;              // 8 KB: one 64-row TMA box of activations
+constexpr int kStage = 2 * kATile + (kBN / 64) * kBBox;   // 64 KB
+constexpr int kThreads = 192;
+
+struct TcParams {
+    CUtensorMap tmA0;     // phase 1: gate [E][I][H]; phase 2: down [E][H][I]
+    CUtensorMap tmA1;     // phase 1: up; phase 2: unused (down again)
+    CUtensorMap tmB;      // sorted activations [Tk][K]
+    GemmArgs a;
+};
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
+// apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;             // version
+    d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A/B f16 (0) or bf16 (1), both K-major.
+__device__ __forceinline__ uint32_t idesc_f16kind(int ab_bf16, int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(ab_bf16) << 7) |
+           (static_cast<uint32_t>(ab_bf16) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                     uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float act_fn(int act, float g, float u, float limit, float alpha) {
+    if (act == ACT_SILU) return g / (1.0f + expf(-g)) * u;
+    if (act == ACT_GELU) {
+        const float c = 0.7978845608028654f;   // sqrt(2/pi)
+        return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g))) * u;
+    }
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
+    return g / (1.0f + expf(-alpha * g)) * (u + 1.0f);
+}
+
+struct SmemTail {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull;
+    uint64_t tempty;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+    int nt;                         // touched experts
+    int touched[kMaxExperts];
+    int cnt[kMaxExperts];
+    int ioff[kMaxExperts + 1];      // item prefix per touched expert
+};
+
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SmemTail* tl = reinterpret_cast<SmemTail*>(base + kStages * kStage);
+    const GemmArgs& a = P.a;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = a.R, K = a.K;
+    const int rows_per_item = a.phase == 0 ? kBM : 2 * kBM;
+    const int MB = (R + rows_per_item - 1) / rows_per_item;
+    const int nkb = K / kBK;
+
+    if (threadIdx.x == 0) {
+        int nt = 0, acc = 0;
+        for (int e = 0; e < a.E; ++e) {
+            const int n = a.off[e + 1] - a.off[e];
+            if (n > 0) {
+                tl->touched[nt] = e;
+                tl->cnt[nt] = n;
+                tl->ioff[nt] = acc;
+                acc += MB * ((n + kBN - 1) / kBN);
+                ++nt;
+            }
+        }
+        tl->ioff[nt] = acc;
+        tl->nt = nt;
+        tl->abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&tl->full[s], 1);
+            mbar_init(&tl->empty[s], 1);
+        }
+        mbar_init(&tl->tfull, 1);
+        mbar_init(&tl->tempty, 4);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        // 512 TMEM columns: accumulator 0 at column 0, accumulator 1 at column 256
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32(&tl->tmem_base))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tl->tmem_base;
+    const int nt = tl->nt;
+    const int items = tl->ioff[nt];
+
+    auto decode = [&](int i, int& j, int& mb, int& tile) {
+        j = 0;
+        while (j + 1 < nt && i >= tl->ioff[j + 1]) ++j;
+        const int ntl = (tl->cnt[j] + kBN - 1) / kBN;
+        const int local = i - tl->ioff[j];
+        mb = local / ntl;
+        tile = local % ntl;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // =============================== TMA producer ====================================
+            int it = 0;
+            for (int i = blockIdx.x; i < items && !tl->abort_flag; i += gridDim.x) {
+                int j, mb, tile;
+                decode(i, j, mb, tile);
+                const int e = tl->touched[j];
+                const int p0 = a.off[e] + tile * kBN;
+                const int n_valid = min(kBN, tl->cnt[j] - tile * kBN);
+                const int nbox = (n_valid + 63) / 64;
+                const int r0 = mb * rows_per_item;
+                const int r1 = a.phase == 0 ? r0 : r0 + kBM;
+                const uint32_t bytes = 2 * kATile + nbox * kBBox;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait_bounded(&tl->empty[s], ((it / kStages) & 1) ^ 1)) {
+                        tl->abort_flag = 1;
+                        report_error(a.status, DEV_ERR_TIMEOUT);
+                        break;
+                    }
+                    unsigned char* st = base + s * kStage;
+                    mbar_arrive_expect_tx(&tl->full[s], bytes);
+                    tma_load_3d(st, &P.tmA0, kb * kBK, r0, e, &tl->full[s]);
+                    tma_load_3d(st + kATile, a.phase == 0 ? &P.tmA1 : &P.tmA0, kb * kBK, r1, e,
+                                &tl->full[s]);
+                    for (int q = 0; q < nbox; ++q)
+                        tma_load_2d(st + 2 * kATile + q * kBBox, &P.tmB, kb * kBK, p0 + 64 * q,
+                                    &tl->full[s]);
+                }
+            }
+            // drain: the last stages' copies must land before the CTA may exit
+            for (int q = (it > kStages ? it - kStages : 0); q < it; ++q)
+                mbar_wait_bounded(&tl->full[q % kStages], (q / kStages) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ================================= MMA issuer ====================================
+            int it = 0, n_item = 0;
+            for (int i = blockIdx.x; i < items && !tl->abort_flag; i += gridDim.x, ++n_item) {
+                int j, mb, tile;
+                decode(i, j, mb, tile);
+                const int n_valid = min(kBN, tl->cnt[j] - tile * kBN);
+                const int N = (n_valid + 15) & ~15;
+                const uint32_t idesc = idesc_f16kind(a.ab_bf16, kBM, N);
+                if (!mbar_wait_bounded(&tl->tempty, (n_item & 1) ^ 1)) {
+                    tl->abort_flag = 1;
+                    report_error(a.status, DEV_ERR_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait_bounded(&tl->full[s], (it / kStages) & 1)) {
+                        tl->abort_flag = 1;
+                        report_error(a.status, DEV_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(base + s * kStage);
+                    const uint64_t d0 = sdesc_sw128(sa);
+                    const uint64_t d1 = sdesc_sw128(sa + kATile);
+                    const uint64_t db = sdesc_sw128(sa + 2 * kATile);
+#pragma unroll
+                    for (int ks = 0; ks < kBK / 16; ++ks) {
+                        const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+                        umma(tmem, d0 + 2 * ks, db + 2 * ks, idesc, acc);
+                        umma(tmem + 256, d1 + 2 * ks, db + 2 * ks, idesc, acc);
+                    }
+                    umma_commit(&tl->empty[s]);     // frees the stage once these MMAs are done
+                }
+                if (!ok) break;
+                umma_commit(&tl->tfull);            // accumulators ready for the epilogue
+            }
+        }
+    } else {
+        // =================================== epilogue ==========================================
+        const int q = warp & 3;                     // TMEM lane quarter this warp may access
+        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        int n_item = 0;
+        for (int i = blockIdx.x; i < items; i += gridDim.x, ++n_item) {
+            int j, mb, tile;
+            decode(i, j, mb, tile);
+            const int e = tl->touched[j];
+            const int p0 = a.off[e] + tile * kBN;
+            const int n_valid = min(kBN, tl->cnt[j] - tile * kBN);
+            const int N = (n_valid + 15) & ~15;
+            bool ok = !tl->abort_flag && mbar_wait_bounded(&tl->tfull, n_item & 1);
+            if (!ok) {
+                if (lane == 0) {
+                    tl->abort_flag = 1;
+                    report_error(a.status, DEV_ERR_TIMEOUT);
+                }
+                break;
+            }
+            tc_fence_after();
+            if (a.phase == 0) {
+                const int row = mb * kBM + 32 * q + lane;
+                const bool vr = row < R;
+                const size_t bi = static_cast<size_t>(e) * R + (vr ? row : 0);
+                const float bg = a.b0 ? __bfloat162float(__ushort_as_bfloat16(a.b0[bi])) : 0.0f;
+                const float bu = a.b1 ? __bfloat162float(__ushort_as_bfloat16(a.b1[bi])) : 0.0f;
+                uint16_t* hout = static_cast<uint16_t*>(a.out);
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    float g[16], u[16];
+                    tmem_ld16(tq + c0, g);
+                    tmem_ld16(tq + 256 + c0, u);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int c = c0 + t;
+                        if (vr && c < n_valid) {
+                            const float h = act_fn(a.act, g[t] + bg, u[t] + bu, a.limit, a.alpha);
+                            hout[static_cast<size_t>(p0 + c) * R + row] = float_to_adt_bits(h, a.adt);
+                        }
+                    }
+                }
+            } else {
+                const int row0 = mb * 2 * kBM + 32 * q + lane;
+                const int row1 = row0 + kBM;
+                const bool v0 = row0 < R, v1 = row1 < R;
+                const float b0 = (a.b0 && v0) ? __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + row0])) : 0.0f;
+                const float b1 = (a.b0 && v1) ? __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + row1])) : 0.0f;
+                float* eout = static_cast<float*>(a.out);
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    float d0[16], d1[16];
+                    tmem_ld16(tq + c0, d0);
+                    tmem_ld16(tq + 256 + c0, d1);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int c = c0 + t;
+                        if (c < n_valid) {
+                            const size_t r = static_cast<size_t>(a.perm[p0 + c]);
+                            if (v0) eout[r * R + row0] = d0[t] + b0;
+                            if (v1) eout[r * R + row1] = d1[t] + b1;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tl->tempty);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+}
+
+// x rows in route-list order: xs[p] = x[perm[p] / k]
+__global__ void __launch_bounds__(128) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm,
+                                                          int k, int H, int n,
+                                                          uint16_t* __restrict__ xs) {
+    const int p = blockIdx.x;
+    if (p >= n) return;
+    const int t = perm[p] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(p) * H);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool make_map_3d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint64_t R,
+                 uint64_t E, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {K, R, E};
+    const cuuint64_t strides[2] = {K * 2, R * K * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), box_rows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_2d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint64_t rows,
+                 uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, dt_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t tc_gemm_smem_bytes() { return kStages * kStage + sizeof(SmemTail) + 1024; }
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
+                               uint16_t* xs, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    gather_rows_kernel<<<n, 128, 0, s>>>(x, perm, k, H, n, xs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
+    TcParams P;
+    memset(&P, 0, sizeof(P));
+    P.a = a;
+    const int KA = a.K;                 // reduction length
+    const int Rm = a.R;                 // rows per expert matrix
+    if (!make_map_3d(&P.tmA0, a.w0, a.ab_bf16, KA, Rm, a.E, kBM)) return cudaErrorInvalidValue;
+    if (!make_map_3d(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, a.ab_bf16, KA, Rm, a.E, kBM))
+        return cudaErrorInvalidValue;
+    if (!make_map_2d(&P.tmB, a.act_in, a.ab_bf16, KA, a.rows_in, 64)) return cudaErrorInvalidValue;
+    const size_t smem = tc_gemm_smem_bytes();
+    cudaError_t e = ensure_smem(tc_gemm_kernel, smem);
+    if (e != cudaSuccess) return e;
+    tc_gemm_kernel<<<num_sms, kThreads, smem, s>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace tsmoe

@@ -1,0 +1,114 @@
+// internal.h -- launchers and parameter blocks shared between the host API (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tsmoe {
+
+enum { FMT_F16 = 0, FMT_BF16 = 1, FMT_MXFP4 = 2, FMT_INT4 = 3 };
+enum { ACT_SILU = 0, ACT_GELU = 1, ACT_GPTOSS = 2 };
+enum { MODE_SOFTMAX_K = 0, MODE_SIGMOID_BIASED = 1, MODE_SOFTMAX_K_SCALED = 2 };
+
+// error codes written to the device status word (match ts_status)
+enum { DEV_ERR_INVALID = 1, DEV_ERR_TIMEOUT = 4 };
+
+constexpr int kMaxExperts = 256;
+constexpr int kRowTile = 16;   // rows per GEMV unit (the mma M)
+constexpr int kBlockK = 32;    // K elements per quantisation block / GEMV block
+
+// bytes of one packed 16-row x 32-column block: 256 code bytes + scale bytes
+__host__ __device__ constexpr int packed_block_bytes(int fmt) {
+    return fmt == FMT_MXFP4 ? 256 + 16 : 256 + 64;
+}
+
+// ------------------------------------------------------------------------------------------
+// routing
+// ------------------------------------------------------------------------------------------
+struct RouteArgs {
+    const void* x;          // [T][H] adt (router_route) or nullptr
+    const void* Wr;         // [E][H] adt
+    const float* logits_in; // [T][E] (route from logits) or nullptr
+    const float* bias;      // [E] or nullptr
+    const float* scale;     // [E] or nullptr
+    void* xn_out;           // [T][H] adt or nullptr
+    float* logits_out;      // [T][E] or nullptr
+    int32_t* idx;           // [T][k]
+    float* w;               // [T][k]
+    int T, H, E, k, mode, adt, rmsnorm;
+    float eps;
+};
+cudaError_t launch_router(const RouteArgs& a, cudaStream_t s);
+cudaError_t launch_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off,
+                                int32_t* perm, int32_t* inv, int* status, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------
+// streaming GEMV (decode) path
+// ------------------------------------------------------------------------------------------
+struct GemvArgs {
+    int fmt, phase;               // phase 0: gate/up + act -> h ; 1: down -> e (f32)
+    int act;
+    float limit, alpha;
+    const uint8_t* w0;            // gate (phase 0) or down (phase 1), expert 0
+    const uint8_t* w1;            // up (phase 0) or nullptr
+    size_t mat_bytes;             // bytes per expert matrix
+    const uint16_t* b0;           // bias of w0 ([E][R] bf16) or nullptr
+    const uint16_t* b1;           // bias of w1 or nullptr
+    int R, K;                     // rows per expert matrix, reduction length
+    int E;
+    const uint16_t* in;           // phase 0: x [T][K]; phase 1: h [T*k][K] (by route id)
+    int adt;
+    void* out;                    // phase 0: h [T*k][R] adt ; phase 1: e [T*k][R] f32
+    const int32_t* off;           // [E+1] (routed) or nullptr (dense)
+    const int32_t* perm;          // [T*k] (routed) or nullptr
+    int T, k;                     // tokens, routes per token (dense: k = 1)
+    int dense;                    // 1: every token routed to expert 0 (shared expert)
+    int tg;                       // tokens per unit group (1..8)
+    int* status;
+};
+cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s);
+size_t gemv_smem_bytes(int fmt, int K, int tg);
+int gemv_pick_tg(int K);
+
+struct CombineArgs {
+    const float* e;        // [T*k][H] f32 by route id
+    const float* w;        // [T][k]
+    const float* seed;     // [T][H] f32 or nullptr
+    void* y;               // [T][H] adt
+    float* y_f32;          // [T][H] or nullptr
+    int T, H, k, adt;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------
+// tensor-core grouped GEMM (prefill) path
+// ------------------------------------------------------------------------------------------
+struct GemmArgs {
+    int phase;                    // 0: gate/up + act -> h (route-list order); 1: down -> e
+    int ab_bf16;                  // mma operand type: 1 bf16, 0 f16
+    int act;
+    float limit, alpha;
+    int adt;
+    const void* w0;               // canonical 16-bit weights: phase 0 gate, phase 1 down
+    const void* w1;               // phase 0 up
+    const uint16_t* b0;           // bias of w0 ([E][R] bf16) or nullptr
+    const uint16_t* b1;           // bias of w1 or nullptr
+    int R, K, E;                  // rows per expert matrix, reduction length, experts
+    const void* act_in;           // activations in route-list order [rows_in][K]
+    int rows_in;                  // T*k
+    void* out;                    // phase 0: h [T*k][R] (route-list order); 1: e [T*k][R] by id
+    const int32_t* off;           // [E+1]
+    const int32_t* perm;          // [T*k]
+    int* status;
+};
+cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
+                               uint16_t* xs, cudaStream_t s);
+size_t tc_gemm_smem_bytes();
+
+cudaError_t launch_pack(int fmt, int nmat, int R, int K, const uint8_t* codes,
+                        const uint8_t* scales, uint8_t* packed, cudaStream_t s);
+
+}  // namespace tsmoe

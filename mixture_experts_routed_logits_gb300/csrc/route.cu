@@ -1,0 +1,245 @@
+// route.cu -- steps 1-3 of the routed-expert layer on sm_103a:
+//   fused (optional RMSNorm) + router GEMV + bias + top-k + weights, one warp per token, and
+//   the deterministic route-list builder (counting sort by expert).
+//
+// Source pages (docs.rs, turbospark-runtime 0.3.0):
+//   gpt-oss routed-expert pass (src/families/gptoss/moe.rs): module header (bias added to the
+//     logits before the top-k; top-k on the raw biased logits; softmax over the selected k with
+//     no renormalisation, router_topk_gemma4's contract) and the "THE BIAS, BEFORE THE TOP-K"
+//     step of encode_gpt_oss_layer_moe.
+//   Gemma-4 batched routed prefill (src/families/gemma4/moe_batch.rs): router_topk_gemma4 with
+//     per_expert_scale; RMS_EPS; encode_routes (route list for the batched kernels).
+//   Llama/Mixtral decode flow (src/families/llama/mod.rs): "r = family_topk(m @ router)";
+//     MiniMax "biased sigmoid scores with unbiased weights".
+// The pages run the top-k on the host after a blocking readback of the logits; here it stays
+// on the device, so the whole layer is one asynchronous stream of kernels.
+#include "common.cuh"
+
+namespace tsmoe {
+
+namespace {
+
+constexpr int kRouterWarps = 4;
+
+// Order-preserving map of an f32 to u32 (larger float -> larger integer); -0 folds to +0 so
+// that equal keys tie and fall back to the expert id, as the f32 comparison does.
+__device__ __forceinline__ uint32_t mono_u32(float v) {
+    const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Key for a max-reduction: value first, then the LOWER expert id wins a tie.
+__device__ __forceinline__ uint64_t sel_key(float v, int e) {
+    return (static_cast<uint64_t>(mono_u32(v)) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
+}
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
+    uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+    lo = __shfl_xor_sync(0xffffffffu, lo, o);
+    hi = __shfl_xor_sync(0xffffffffu, hi, o);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Fixed-order f32 dot product of a warp: lane l sums fmaf(a[l+32j], b[l+32j]) over j, then an
+// xor butterfly 16, 8, 4, 2, 1.  Every lane returns the same bits.
+template <typename LoadB>
+__device__ __forceinline__ float warp_dot_fixed(const float* a, LoadB loadb, int H, int lane) {
+    float p = 0.0f;
+    for (int j = lane; j < H; j += 32) p = __fmaf_rn(a[j], loadb(j), p);
+    return warp_sum_xor(p);
+}
+
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_kernel(RouteArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRouterWarps + warp;
+    const int E = a.E, H = a.H, k = a.k;
+    // per-warp smem: xs[H] f32 (only with x), key[E], sg[E], ex[k]
+    float* base = reinterpret_cast<float*>(smem_raw);
+    const int xs_len = a.x ? H : 0;
+    const int per_warp = xs_len + 2 * kMaxExperts + kMaxExperts;
+    float* xs = base + warp * per_warp;
+    float* key = xs + xs_len;
+    float* sg = key + kMaxExperts;
+    float* ex = sg + kMaxExperts;
+    __shared__ int sel_s[kRouterWarps][kMaxExperts];
+    if (t >= a.T) return;
+
+    // ---- step 1: optional RMSNorm + raw logits ------------------------------------------
+    if (a.x) {
+        const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * H;
+        for (int j = lane; j < H; j += 32) xs[j] = adt_bits_to_float(xr[j], a.adt);
+        if (a.rmsnorm) {
+            const float ss = warp_dot_fixed(xs, [&](int j) { return xs[j]; }, H, lane);
+            const float ms = __fdiv_rn(ss, static_cast<float>(H));
+            const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+            uint16_t* xo = static_cast<uint16_t*>(a.xn_out) + static_cast<size_t>(t) * H;
+            for (int j = lane; j < H; j += 32) {
+                const uint16_t b = float_to_adt_bits(__fmul_rn(xs[j], r), a.adt);
+                xo[j] = b;
+                xs[j] = adt_bits_to_float(b, a.adt);
+            }
+        }
+        const uint16_t* W = static_cast<const uint16_t*>(a.Wr);
+        for (int e = 0; e < E; ++e) {
+            const uint16_t* wr = W + static_cast<size_t>(e) * H;
+            const float l = warp_dot_fixed(xs, [&](int j) { return adt_bits_to_float(wr[j], a.adt); },
+                                           H, lane);
+            if (lane == 0) key[e] = l;   // raw logit for now
+        }
+        __syncwarp();
+    } else {
+        const float* lr = a.logits_in + static_cast<size_t>(t) * E;
+        for (int e = lane; e < E; e += 32) key[e] = lr[e];
+        __syncwarp();
+    }
+
+    // ---- step 2: keys per mode --------------------------------------------------------------
+    for (int e = lane; e < E; e += 32) {
+        const float l = key[e];
+        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
+        const float b = a.bias ? a.bias[e] : 0.0f;
+        float kv;
+        if (a.mode == MODE_SIGMOID_BIASED) {
+            const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
+            sg[e] = s;
+            kv = a.bias ? __fadd_rn(s, b) : s;
+        } else {
+            kv = a.bias ? __fadd_rn(l, b) : l;
+        }
+        key[e] = kv;
+    }
+    __syncwarp();
+
+    // top-k by repeated warp arg-max; each lane owns experts lane + 32 i
+    uint64_t own[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        own[i] = e < E ? sel_key(key[e], e) : 0ull;
+    }
+    for (int s = 0; s < k; ++s) {
+        uint64_t best = 0ull;
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) best = own[i] > best ? own[i] : best;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const uint64_t other = shfl_xor_u64(best, o);
+            best = other > best ? other : best;
+        }
+        const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+        if ((e & 31) == lane) {
+#pragma unroll
+            for (int i = 0; i < kMaxExperts / 32; ++i)
+                if (lane + 32 * i == e) own[i] = 0ull;
+        }
+        if (lane == 0) sel_s[warp][s] = e;
+    }
+    __syncwarp();
+
+    // ---- weights ------------------------------------------------------------------------------
+    const int* sel = sel_s[warp];
+    if (a.mode == MODE_SIGMOID_BIASED) {
+        for (int s = lane; s < k; s += 32) ex[s] = sg[sel[s]];
+    } else {
+        const float m = key[sel[0]];
+        for (int s = lane; s < k; s += 32) ex[s] = expf(__fsub_rn(key[sel[s]], m));
+    }
+    __syncwarp();
+    float sum = 0.0f;
+    if (lane == 0)
+        for (int s = 0; s < k; ++s) sum = __fadd_rn(sum, ex[s]);   // slot order
+    sum = __shfl_sync(0xffffffffu, sum, 0);
+    for (int s = lane; s < k; s += 32) {
+        float wv = __fdiv_rn(ex[s], sum);
+        if (a.mode == MODE_SOFTMAX_K_SCALED) wv = __fmul_rn(wv, a.scale[sel[s]]);
+        a.idx[static_cast<size_t>(t) * k + s] = sel[s];
+        a.w[static_cast<size_t>(t) * k + s] = wv;
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Route list: off[E+1], perm (route ids grouped by expert, ascending id inside an expert),
+// inv.  One CTA, deterministic: counts, exclusive scan, then a stable scatter in chunks of
+// 1024 routes (rank inside a chunk from warp match masks plus earlier warps' counts).
+// ------------------------------------------------------------------------------------------
+constexpr int kBuildThreads = 1024;
+
+__global__ void __launch_bounds__(kBuildThreads)
+build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __restrict__ off,
+                    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int* status) {
+    __shared__ int cnt[kMaxExperts];
+    __shared__ int cursor[kMaxExperts];
+    __shared__ int wcnt[kBuildThreads / 32][kMaxExperts];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int e = tid; e < E; e += kBuildThreads) cnt[e] = 0;
+    __syncthreads();
+    for (int r = tid; r < n; r += kBuildThreads) {
+        const int e = idx[r];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else report_error(status, DEV_ERR_INVALID);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = acc;
+            cursor[e] = acc;
+            acc += cnt[e];
+        }
+        off[E] = acc;
+    }
+    __syncthreads();
+    for (int base = 0; base < n; base += kBuildThreads) {
+        for (int i = tid; i < (kBuildThreads / 32) * E; i += kBuildThreads)
+            wcnt[i / E][i % E] = 0;
+        __syncthreads();
+        const int r = base + tid;
+        int e = -1;
+        if (r < n) {
+            e = idx[r];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
+        __syncthreads();
+        if (e >= 0) {
+            int pos = cursor[e] + rank;
+            for (int w2 = 0; w2 < warp; ++w2) pos += wcnt[w2][e];
+            perm[pos] = r;
+            inv[r] = pos;
+        }
+        __syncthreads();
+        for (int e2 = tid; e2 < E; e2 += kBuildThreads) {
+            int add = 0;
+            for (int w2 = 0; w2 < kBuildThreads / 32; ++w2) add += wcnt[w2][e2];
+            cursor[e2] += add;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
+    if (a.T <= 0) return cudaSuccess;
+    const int xs_len = a.x ? a.H : 0;
+    const size_t smem = static_cast<size_t>(kRouterWarps) * (xs_len + 3 * kMaxExperts) * 4;
+    if (smem > 48 * 1024) {
+        cudaError_t e = ensure_smem(router_kernel, smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int grid = (a.T + kRouterWarps - 1) / kRouterWarps;
+    router_kernel<<<grid, kRouterWarps * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off,
+                                int32_t* perm, int32_t* inv, int* status, cudaStream_t s) {
+    build_routes_kernel<<<1, kBuildThreads, 0, s>>>(idx, T * k, E, off, perm, inv, status);
+    return cudaGetLastError();
+}
+
+}  // namespace tsmoe

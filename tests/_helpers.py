@@ -58,3 +58,76 @@ def np_dequant(fmt: str, codes, scales=None) -> np.ndarray:
         m = np.repeat(sm[..., 1], 32, axis=-1)
         return q.astype(np.float64) * s + m
     raise ValueError(fmt)
+
+
+# ------------------------------------------------------------------ layer -> oracle + GPU
+def oracle_layer(L):
+    """Oracle descriptors for a synth layer (tensors may live on any device)."""
+    c = L["cfg"]
+    ex = oracle_experts(L["experts"], c["fmt"], c["act"], c["E"], c["H"], c["I"])
+    sh = (oracle_experts(L["shared"], "f16", c["act"], 1, c["H"], c["shared_I"])
+          if L.get("shared") is not None else None)
+    return ex, sh
+
+
+def to_device(L, device="cuda"):
+    """A copy of a synth layer with every tensor moved to `device`."""
+    out = {}
+    for key, v in L.items():
+        if isinstance(v, torch.Tensor):
+            out[key] = v.to(device)
+        elif isinstance(v, dict) and key in ("experts", "shared"):
+            out[key] = {n: (t.to(device) if isinstance(t, torch.Tensor) else t) for n, t in v.items()}
+        else:
+            out[key] = v
+    return out
+
+
+def gpu_layer(L):
+    """Library Experts (packed where needed) for a synth layer whose tensors are on the GPU."""
+    import mixture_experts_routed_logits_gb300 as moe
+    c = L["cfg"]
+    ex = moe.Experts.from_canonical(c["fmt"], c["act"], L["experts"])
+    sh = (moe.Experts.from_canonical("f16", c["act"], L["shared"])
+          if L.get("shared") is not None else None)
+    return ex, sh
+
+
+def oracle_route(L, x_bits):
+    """Oracle steps a0-a2 for a layer: (xn bits or None, logits, idx, w)."""
+    c = L["cfg"]
+    xn = oracle.rmsnorm(x_bits, c["adt"], 1e-6) if c["rmsnorm"] else None
+    lg = oracle.router_logits(xn if xn is not None else x_bits, bits16(L["Wr"]), c["adt"])
+    bias = None if L["router_bias"] is None else L["router_bias"].cpu().numpy()
+    scale = None if L["scale"] is None else L["scale"].cpu().numpy()
+    idx, w = oracle.route(lg, c["k"], c["mode"], bias=bias, scale=scale)
+    return xn, lg, idx, w
+
+
+def parity_metrics(y_gpu_f64, y_ref_f64):
+    d = np.abs(y_gpu_f64 - y_ref_f64)
+    rel = np.linalg.norm(y_gpu_f64 - y_ref_f64) / max(np.linalg.norm(y_ref_f64), 1e-30)
+    return float(d.max()), float(rel)
+
+
+def ulp16(v, adt):
+    """One unit in the last place of the 16-bit activation type at |v| (numpy, float64)."""
+    v = np.abs(np.asarray(v, np.float64))
+    p = 8 if adt == "bf16" else 11
+    emin = -126 if adt == "bf16" else -14
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** emin)))
+    return np.ldexp(1.0, (e - (p - 1)).astype(np.int64))
+
+
+def check_outputs(y_gpu_f64, y32_gpu_f64, y_ref_bits_f64, y32_ref_f64, adt, max_abs=2e-2, rel_l2=1e-3):
+    """The parity bar: f32 outputs within max-abs and rel-L2; 16-bit outputs within the same
+    bars, except that an element may differ by one unit in the last place of the 16-bit type
+    (both sides round an f32 sum; sums a hair apart can straddle a rounding boundary)."""
+    mx, rel = parity_metrics(y32_gpu_f64, y32_ref_f64)
+    assert mx <= max_abs and rel <= rel_l2, ("f32 outputs", mx, rel)
+    d = np.abs(y_gpu_f64 - y_ref_bits_f64)
+    allow = np.maximum(max_abs, ulp16(y_ref_bits_f64, adt))
+    assert np.all(d <= allow), ("16-bit outputs", float(d.max()))
+    rel16 = np.linalg.norm(y_gpu_f64 - y_ref_bits_f64) / max(np.linalg.norm(y_ref_bits_f64), 1e-30)
+    assert rel16 <= rel_l2, ("16-bit rel-L2", rel16)
+    return mx, rel
