@@ -30,9 +30,18 @@ inline cudaError_t ensure_smem(K kernel, size_t bytes) {
     for (int i = 0; i < used; ++i)
         if (table[i].fn == fn && table[i].dev == dev && table[i].bytes >= static_cast<int>(bytes))
             return cudaSuccess;
-    const int want = 227 * 1024 > static_cast<int>(bytes) ? 227 * 1024 : static_cast<int>(bytes);
+    // raise the limit once to the most this kernel can use (opt-in maximum minus its static
+    // shared memory), so that later, larger requests need no further attribute call
+    cudaFuncAttributes fa;
+    int optin = 0;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return e; }
+    const int want = optin - static_cast<int>(fa.sharedSizeBytes);
+    if (static_cast<int>(bytes) > want) return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
-    if (e == cudaSuccess && used < 64) table[used++] = Slot{fn, dev, want};
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return e; }
+    if (used < 64) table[used++] = Slot{fn, dev, want};
     return e;
 }
 
