@@ -78,9 +78,12 @@ typedef enum { TS_ACT_SILU_GLU = 0, TS_ACT_GELU_TANH_GLU = 1, TS_ACT_GPTOSS_SWIG
 /* Path selection for ts_moe_forward_path. */
 typedef enum {
     TS_PATH_AUTO = 0,  /* GEMV path for T <= 8 tokens, else the tensor-core grouped GEMM when the
-                          format has one (bf16, MXFP4), else the GEMV path                     */
+                          format has one (MXFP4, or f16/bf16 weights of the activation type)
+                          and H, I are multiples of 64, else the GEMV path                      */
     TS_PATH_GEMV = 1,  /* streaming GEMV kernels (any T)                                        */
-    TS_PATH_GEMM = 2   /* tcgen05 grouped GEMM (bf16 and MXFP4 weights only)                    */
+    TS_PATH_GEMM = 2   /* tcgen05 grouped GEMM.  MXFP4 weights are dequantised to f16 in shared
+                          memory, exact for e8m0 scales 2^-23..2^13; a block outside that range
+                          makes ts_moe_device_status report TS_ERR_UNSUPPORTED               */
 } ts_path;
 
 /* One set of experts (routed experts, or the shared expert with E = 1).

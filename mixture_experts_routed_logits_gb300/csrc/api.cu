@@ -89,7 +89,7 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
 }
 
 struct WsLayout {
-    size_t status, off, perm, inv, h, e, hs, s, xs, total;
+    size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hmax, hinv, h16, total;
 };
 
 WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts* sh) {
@@ -112,6 +112,12 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
         L.s = take(static_cast<size_t>(T) * ex->H * 4);
     }
     L.xs = take(Tk * ex->H * 2);   // activations in route-list order (tensor-core path)
+    if (ex->fmt == FMT_MXFP4) {      // f16 operands of the MXFP4 tensor-core path
+        L.xinv = take(Tk * 4);
+        L.hmax = take(Tk * 4);
+        L.hinv = take(Tk * 4);
+        L.h16 = take(Tk * ex->I * 2);
+    }
     L.total = a;
     return L;
 }
@@ -279,12 +285,14 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     const bool gemm_fmt = (ex->fmt == FMT_BF16 && adt == TS_DT_BF16) ||
                           (ex->fmt == FMT_F16 && adt == TS_DT_F16);
     const bool gemm_shape = ex->H % 64 == 0 && ex->I % 64 == 0;
-    if (path == TS_PATH_GEMM && !(gemm_fmt && gemm_shape))
+    const bool quant_gemm = ex->fmt == FMT_MXFP4;
+    if (path == TS_PATH_GEMM && !((gemm_fmt || quant_gemm) && gemm_shape))
         return fail(TS_ERR_UNSUPPORTED,
-                    "%s: the tensor-core path serves 16-bit weights of the activation type with "
-                    "H %% 64 == 0 and I %% 64 == 0 (fmt=%d adt=%d H=%d I=%d)", what, ex->fmt, adt,
-                    ex->H, ex->I);
-    const bool use_gemm = path == TS_PATH_GEMM || (path == TS_PATH_AUTO && T > 8 && gemm_fmt && gemm_shape);
+                    "%s: the tensor-core path serves MXFP4 weights or 16-bit weights of the "
+                    "activation type, with H %% 64 == 0 and I %% 64 == 0 (fmt=%d adt=%d H=%d I=%d)",
+                    what, ex->fmt, adt, ex->H, ex->I);
+    const bool use_gemm = path == TS_PATH_GEMM ||
+                          (path == TS_PATH_AUTO && T > 8 && (gemm_fmt || quant_gemm) && gemm_shape);
 
     unsigned char* W = static_cast<unsigned char*>(ws);
     int* status = reinterpret_cast<int*>(W + L.status);
@@ -299,42 +307,64 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     if (use_gemm) {
         const int sms = num_sms_current();
         if (sms <= 0) return fail(TS_ERR_CUDA, "%s: no CUDA device", what);
+        const int Tk = T * k;
         uint16_t* xs = reinterpret_cast<uint16_t*>(W + L.xs);
-        e = launch_gather_rows(static_cast<const uint16_t*>(x), perm, k, ex->H, T * k, xs, st);
+        float* xinv = quant_gemm ? reinterpret_cast<float*>(W + L.xinv) : nullptr;
+        unsigned* hmax = quant_gemm ? reinterpret_cast<unsigned*>(W + L.hmax) : nullptr;
+        if (quant_gemm)
+            e = launch_gather_rows_f16(static_cast<const uint16_t*>(x), adt, perm, k, ex->H, Tk, xs,
+                                       xinv, hmax, st);
+        else
+            e = launch_gather_rows(static_cast<const uint16_t*>(x), perm, k, ex->H, Tk, xs, st);
         if (e == cudaSuccess) e = phase_mark(0, st);
         if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: gather");
         GemmArgs G{};
         G.phase = 0;
-        G.ab_bf16 = adt == TS_DT_BF16 ? 1 : 0;
+        G.quant = quant_gemm ? 1 : 0;
+        G.ab_bf16 = (!quant_gemm && adt == TS_DT_BF16) ? 1 : 0;
         G.act = ex->act;
         G.limit = ex->swiglu_limit;
         G.alpha = ex->swiglu_alpha;
         G.adt = adt;
         G.w0 = ex->gate;
         G.w1 = ex->up;
+        G.mat_bytes = matrix_bytes(ex->fmt, ex->I, ex->H);
         G.b0 = static_cast<const uint16_t*>(ex->gate_b);
         G.b1 = static_cast<const uint16_t*>(ex->up_b);
         G.R = ex->I;
         G.K = ex->H;
         G.E = ex->E;
         G.act_in = xs;
-        G.rows_in = T * k;
+        G.rows_in = Tk;
         G.out = W + L.h;
         G.off = off;
         G.perm = perm;
         G.status = status;
+        G.col_scale = xinv;
+        G.hmax = hmax;
         e = launch_tc_gemm(G, sms, st);
         if (e == cudaSuccess) e = phase_mark(1, st);
         if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: tensor-core phase 1");
         G.phase = 1;
         G.w0 = ex->down;
         G.w1 = nullptr;
+        G.mat_bytes = matrix_bytes(ex->fmt, ex->H, ex->I);
         G.b0 = static_cast<const uint16_t*>(ex->down_b);
         G.b1 = nullptr;
         G.R = ex->H;
         G.K = ex->I;
         G.act_in = W + L.h;
         G.out = W + L.e;
+        G.hmax = nullptr;
+        if (quant_gemm) {
+            uint16_t* h16 = reinterpret_cast<uint16_t*>(W + L.h16);
+            float* hinv = reinterpret_cast<float*>(W + L.hinv);
+            e = launch_h_to_f16(reinterpret_cast<const uint16_t*>(W + L.h), adt, hmax, ex->I, Tk, h16,
+                                hinv, st);
+            if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: h to f16");
+            G.act_in = h16;
+            G.col_scale = hinv;
+        }
         e = launch_tc_gemm(G, sms, st);
         if (e == cudaSuccess) e = phase_mark(3, st);
         if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: tensor-core phase 2");

@@ -174,6 +174,19 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
     return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
 }
 
+// Four bytes of e2m1 pairs (byte j -> out[j]: low nibble in .x, high nibble in .y) with the
+// hardware converter, from one 32-bit register.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t out[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(w));
+}
+
 // Unsigned 4-bit codes to f16x2 via the 1024-offset trick: (0x6400 | q) is the f16 1024+q.
 // Returns the pair (nibble at bit s, nibble at bit s+16) as f16 values q, exactly.
 __device__ __forceinline__ uint32_t u4pair_to_f16x2(uint32_t w, int s) {

@@ -24,6 +24,13 @@
 //   * Warp roles: warp 0 = TMA producer (3-stage ring of 64 KB), warp 1 = MMA issuer (one
 //     thread, tcgen05.mma kind::f16, 128B-swizzled K-major smem descriptors), warps 2-5 =
 //     epilogue (tcgen05.ld of their TMEM lane quarter).  Every mbarrier wait is bounded.
+//   * MXFP4 weights (QUANT variant): the producer bulk-copies the packed e2m1 tiles (with their
+//     e8m0 block scales) into a staging area of each stage; four dequant warps turn them into
+//     f16 (hardware e2m1x2 -> f16x2 convert, times the block scale, exact while the scale is in
+//     [2^-23, 2^13]; outside it the device status reports TS_ERR_UNSUPPORTED) written straight into the 128B-swizzled A tile; the MMA waits on a
+//     "dequantised" barrier instead of the copy barrier.  Activations enter as f16 with a
+//     per-route power-of-two prescale that the epilogue undoes.  Each weight element crosses HBM
+//     once per route tile, as packed bytes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,6 +48,13 @@ constexpr int kATile = kBM * kBK * 2;            // 16 KB
 constexpr int kBBox = 64 * kBK * 2;              // 8 KB: one 64-row TMA box of activations
 constexpr int kStage = 2 * kATile + (kBN / 64) * kBBox;   // 64 KB
 constexpr int kThreads = 192;
+// QUANT variant: + staging of the packed tiles (2 tiles x 8 row tiles x 2 blocks x 272 B),
+// stage rounded to 1 KB so every A tile stays 1024-byte aligned for the 128B swizzle
+constexpr int kPackBlk = 272;
+constexpr int kStaging = 2 * 8 * 2 * kPackBlk;             // 8704 B
+constexpr int kStageQ = (kStage + kStaging + 1023) / 1024 * 1024;
+constexpr int kThreadsQ = 320;                              // + 4 dequant warps
+constexpr int kDqWarps = 4;
 
 struct TcParams {
     CUtensorMap tmA0;     // phase 1: gate [E][I][H]; phase 2: down [E][H][I]
@@ -136,6 +150,7 @@ __device__ __forceinline__ float act_fn(int act, float g, float u, float limit, 
 struct SmemTail {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t dq[kStages];           // QUANT: A tiles dequantised
     uint64_t tfull;
     uint64_t tempty;
     uint32_t tmem_base;
@@ -146,11 +161,14 @@ struct SmemTail {
     int ioff[kMaxExperts + 1];      // item prefix per touched expert
 };
 
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams P) {
+template <bool QUANT>
+__global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
+    constexpr int SB = QUANT ? kStageQ : kStage;            // bytes per stage
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SmemTail* tl = reinterpret_cast<SmemTail*>(base + kStages * kStage);
+    SmemTail* tl = reinterpret_cast<SmemTail*>(base + kStages * SB);
     const GemmArgs& a = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = a.R, K = a.K;
@@ -176,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&tl->full[s], 1);
             mbar_init(&tl->empty[s], 1);
+            mbar_init(&tl->dq[s], kDqWarps);
         }
         mbar_init(&tl->tfull, 1);
         mbar_init(&tl->tempty, 4);
@@ -217,7 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 const int nbox = (n_valid + 63) / 64;
                 const int r0 = mb * rows_per_item;
                 const int r1 = a.phase == 0 ? r0 : r0 + kBM;
-                const uint32_t bytes = 2 * kATile + nbox * kBBox;
+                const int RT = R / kRowTile;                // 16-row tiles per expert matrix
+                const int nblk = K / kBlockK;
+                int nq = 0;                                 // packed row tiles copied per stage
+                if (QUANT) {
+                    for (int t = 0; t < 8; ++t) nq += (r0 / kRowTile + t < RT) + (r1 / kRowTile + t < RT);
+                }
+                const uint32_t bytes = (QUANT ? nq * 2 * kPackBlk : 2 * kATile) + nbox * kBBox;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait_bounded(&tl->empty[s], ((it / kStages) & 1) ^ 1)) {
@@ -225,11 +250,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                         report_error(a.status, DEV_ERR_TIMEOUT);
                         break;
                     }
-                    unsigned char* st = base + s * kStage;
+                    unsigned char* st = base + s * SB;
                     mbar_arrive_expect_tx(&tl->full[s], bytes);
-                    tma_load_3d(st, &P.tmA0, kb * kBK, r0, e, &tl->full[s]);
-                    tma_load_3d(st + kATile, a.phase == 0 ? &P.tmA1 : &P.tmA0, kb * kBK, r1, e,
-                                &tl->full[s]);
+                    if (QUANT) {
+                        unsigned char* stg = st + kStage;
+                        const uint8_t* m0 = static_cast<const uint8_t*>(a.w0) + static_cast<size_t>(e) * a.mat_bytes;
+                        const uint8_t* m1 = static_cast<const uint8_t*>(a.phase == 0 ? a.w1 : a.w0) +
+                                            static_cast<size_t>(e) * a.mat_bytes;
+                        for (int t = 0; t < 8; ++t) {
+                            const int rta = r0 / kRowTile + t, rtb = r1 / kRowTile + t;
+                            if (rta < RT)
+                                bulk_g2s(stg + t * 2 * kPackBlk,
+                                         m0 + (static_cast<size_t>(rta) * nblk + 2 * kb) * kPackBlk,
+                                         2 * kPackBlk, &tl->full[s]);
+                            if (rtb < RT)
+                                bulk_g2s(stg + (8 + t) * 2 * kPackBlk,
+                                         m1 + (static_cast<size_t>(rtb) * nblk + 2 * kb) * kPackBlk,
+                                         2 * kPackBlk, &tl->full[s]);
+                        }
+                    } else {
+                        tma_load_3d(st, &P.tmA0, kb * kBK, r0, e, &tl->full[s]);
+                        tma_load_3d(st + kATile, a.phase == 0 ? &P.tmA1 : &P.tmA0, kb * kBK, r1, e,
+                                    &tl->full[s]);
+                    }
                     for (int q = 0; q < nbox; ++q)
                         tma_load_2d(st + 2 * kATile + q * kBBox, &P.tmB, kb * kBK, p0 + 64 * q,
                                     &tl->full[s]);
@@ -258,14 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % kStages;
-                    if (!mbar_wait_bounded(&tl->full[s], (it / kStages) & 1)) {
+                    if (!mbar_wait_bounded(QUANT ? &tl->dq[s] : &tl->full[s], (it / kStages) & 1)) {
                         tl->abort_flag = 1;
                         report_error(a.status, DEV_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(base + s * kStage);
+                    const uint32_t sa = smem_u32(base + s * SB);
                     const uint64_t d0 = sdesc_sw128(sa);
                     const uint64_t d1 = sdesc_sw128(sa + kATile);
                     const uint64_t db = sdesc_sw128(sa + 2 * kATile);
@@ -281,6 +324,61 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 umma_commit(&tl->tfull);            // accumulators ready for the epilogue
             }
         }
+    } else if (QUANT && warp >= 6) {
+        // ======================= dequant warps (QUANT): packed e2m1 -> f16 A tiles =============
+        const int dw = warp - 6;
+        const int gid = lane >> 2, tid = lane & 3;
+        int it = 0;
+        bool bad_scale = false;
+        for (int i = blockIdx.x; i < items && !tl->abort_flag; i += gridDim.x) {
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int s = it % kStages;
+                if (!mbar_wait_bounded(&tl->full[s], (it / kStages) & 1)) {
+                    if (lane == 0) {
+                        tl->abort_flag = 1;
+                        report_error(a.status, DEV_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                unsigned char* st = base + s * SB;
+                const unsigned char* stg = st + kStage;
+#pragma unroll 2
+                for (int qb = dw; qb < 32; qb += kDqWarps) {
+                    const int tile = qb >> 4, rt = (qb >> 1) & 7, bb = qb & 1;
+                    const unsigned char* blk = stg + (tile * 8 + rt) * 2 * kPackBlk + bb * kPackBlk;
+                    const uint2 cw = *reinterpret_cast<const uint2*>(blk + lane * 8);
+                    const uint32_t sc = *reinterpret_cast<const uint16_t*>(blk + 256 + gid * 2);
+                    const uint32_t e0 = sc & 0xFF, e1 = sc >> 8;
+                    // scaled e2m1 values are exact f16 numbers only for scales 2^-23 .. 2^13
+                    bad_scale |= (e0 < 104u) | (e0 > 140u) | (e1 < 104u) | (e1 > 140u);
+                    const __half2 s0 = __half2half2(__float2half_rn(e8m0_to_float(e0)));
+                    const __half2 s1 = __half2half2(__float2half_rn(e8m0_to_float(e1)));
+                    uint32_t va[4], vb[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t ra = e2m1x2_to_f16x2(cw.x >> (8 * j));
+                        uint32_t rb = e2m1x2_to_f16x2(cw.y >> (8 * j));
+                        __half2 ha = __hmul2(*reinterpret_cast<__half2*>(&ra), s0);
+                        __half2 hb = __hmul2(*reinterpret_cast<__half2*>(&rb), s1);
+                        va[j] = *reinterpret_cast<uint32_t*>(&ha);
+                        vb[j] = *reinterpret_cast<uint32_t*>(&hb);
+                    }
+                    // 128B swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
+                    unsigned char* at = st + tile * kATile;
+                    const int ra_row = rt * kRowTile + gid, rb_row = ra_row + 8;
+                    const int c = 4 * bb + tid;
+                    *reinterpret_cast<uint4*>(at + ra_row * 128 + ((c ^ (ra_row & 7)) << 4)) =
+                        make_uint4(va[0], va[1], va[2], va[3]);
+                    *reinterpret_cast<uint4*>(at + rb_row * 128 + ((c ^ (rb_row & 7)) << 4)) =
+                        make_uint4(vb[0], vb[1], vb[2], vb[3]);
+                }
+                // generic-proxy stores must be visible to the tensor core's async-proxy reads
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tl->dq[s]);
+            }
+        }
+        if (__any_sync(0xffffffffu, bad_scale) && lane == 0) report_error(a.status, DEV_ERR_UNSUPPORTED);
     } else {
         // =================================== epilogue ==========================================
         const int q = warp & 3;                     // TMEM lane quarter this warp may access
@@ -317,8 +415,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                     for (int t = 0; t < 16; ++t) {
                         const int c = c0 + t;
                         if (vr && c < n_valid) {
-                            const float h = act_fn(a.act, g[t] + bg, u[t] + bu, a.limit, a.alpha);
-                            hout[static_cast<size_t>(p0 + c) * R + row] = float_to_adt_bits(h, a.adt);
+                            float gv = g[t], uv = u[t];
+                            if (QUANT) {
+                                const float inv = a.col_scale[p0 + c];
+                                gv *= inv;
+                                uv *= inv;
+                            }
+                            const float h = act_fn(a.act, gv + bg, uv + bu, a.limit, a.alpha);
+                            const uint16_t hb = float_to_adt_bits(h, a.adt);
+                            hout[static_cast<size_t>(p0 + c) * R + row] = hb;
+                            if (QUANT)
+                                atomicMax(a.hmax + p0 + c, __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt))));
                         }
                     }
                 }
@@ -338,8 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                         const int c = c0 + t;
                         if (c < n_valid) {
                             const size_t r = static_cast<size_t>(a.perm[p0 + c]);
-                            if (v0) eout[r * R + row0] = d0[t] + b0;
-                            if (v1) eout[r * R + row1] = d1[t] + b1;
+                            const float inv = QUANT ? a.col_scale[p0 + c] : 1.0f;
+                            if (v0) eout[r * R + row0] = d0[t] * inv + b0;
+                            if (v1) eout[r * R + row1] = d1[t] * inv + b1;
                         }
                     }
                 }
@@ -367,6 +475,68 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint16_t* __rest
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
     uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(p) * H);
     for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+// Power-of-two prescale for an f16 operand: 2^ks with max|v| * 2^ks in [2^14, 2^15).
+__device__ __forceinline__ void prescale_of(float mx, float& scl, float& inv) {
+    scl = inv = 1.0f;
+    if (mx > 0.0f && mx < 3.0e38f) {
+        int ex;
+        frexpf(mx, &ex);
+        int ks = max(-120, min(120, 15 - ex));
+        scl = __uint_as_float(static_cast<uint32_t>(ks + 127) << 23);
+        inv = __uint_as_float(static_cast<uint32_t>(127 - ks) << 23);
+    }
+}
+
+__device__ __forceinline__ float block_max128(float v, float* red) {
+    v = warp_max(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    const float m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+    return m;
+}
+
+// Route-ordered activations for the f16 tensor-core operand: xs[p] = f16(x[perm[p]/k] * 2^ks),
+// inv[p] = 2^-ks; also clears hmax[p] for the phase-1 epilogue.
+__global__ void __launch_bounds__(128) gather_rows_f16_kernel(const uint16_t* __restrict__ x, int adt,
+                                                              const int32_t* __restrict__ perm, int k,
+                                                              int H, int n, uint16_t* __restrict__ xs,
+                                                              float* __restrict__ inv_out,
+                                                              unsigned* __restrict__ hmax) {
+    __shared__ float red[4];
+    const int p = blockIdx.x;
+    if (p >= n) return;
+    const uint16_t* src = x + static_cast<size_t>(perm[p] / k) * H;
+    float mx = 0.0f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) mx = fmaxf(mx, fabsf(adt_bits_to_float(src[i], adt)));
+    mx = block_max128(mx, red);
+    float scl, inv;
+    prescale_of(mx, scl, inv);
+    uint16_t* dst = xs + static_cast<size_t>(p) * H;
+    for (int i = threadIdx.x; i < H; i += blockDim.x)
+        dst[i] = __half_as_ushort(__float2half_rn(__fmul_rn(adt_bits_to_float(src[i], adt), scl)));
+    if (threadIdx.x == 0) {
+        inv_out[p] = inv;
+        hmax[p] = 0u;
+    }
+}
+
+// h (16-bit, route order) -> f16 with a per-route prescale from hmax[p].
+__global__ void __launch_bounds__(128) h_to_f16_kernel(const uint16_t* __restrict__ h, int adt,
+                                                       const unsigned* __restrict__ hmax, int I, int n,
+                                                       uint16_t* __restrict__ h16,
+                                                       float* __restrict__ inv_out) {
+    const int p = blockIdx.x;
+    if (p >= n) return;
+    float scl, inv;
+    prescale_of(__uint_as_float(hmax[p]), scl, inv);
+    const uint16_t* src = h + static_cast<size_t>(p) * I;
+    uint16_t* dst = h16 + static_cast<size_t>(p) * I;
+    for (int i = threadIdx.x; i < I; i += blockDim.x)
+        dst[i] = __half_as_ushort(__float2half_rn(__fmul_rn(adt_bits_to_float(src[i], adt), scl)));
+    if (threadIdx.x == 0) inv_out[p] = inv;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -412,12 +582,26 @@ bool make_map_2d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint
 
 }  // namespace
 
-size_t tc_gemm_smem_bytes() { return kStages * kStage + sizeof(SmemTail) + 1024; }
+size_t tc_gemm_smem_bytes() { return kStages * kStageQ + sizeof(SmemTail) + 1024; }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
                                uint16_t* xs, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     gather_rows_kernel<<<n, 128, 0, s>>>(x, perm, k, H, n, xs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows_f16(const uint16_t* x, int adt, const int32_t* perm, int k, int H,
+                                   int n, uint16_t* xs, float* inv, unsigned* hmax, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    gather_rows_f16_kernel<<<n, 128, 0, s>>>(x, adt, perm, k, H, n, xs, inv, hmax);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_h_to_f16(const uint16_t* h, int adt, const unsigned* hmax, int I, int n,
+                            uint16_t* h16, float* inv, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    h_to_f16_kernel<<<n, 128, 0, s>>>(h, adt, hmax, I, n, h16, inv);
     return cudaGetLastError();
 }
 
@@ -427,14 +611,24 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     P.a = a;
     const int KA = a.K;                 // reduction length
     const int Rm = a.R;                 // rows per expert matrix
-    if (!make_map_3d(&P.tmA0, a.w0, a.ab_bf16, KA, Rm, a.E, kBM)) return cudaErrorInvalidValue;
-    if (!make_map_3d(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, a.ab_bf16, KA, Rm, a.E, kBM))
-        return cudaErrorInvalidValue;
+    if (!a.quant) {
+        if (!make_map_3d(&P.tmA0, a.w0, a.ab_bf16, KA, Rm, a.E, kBM)) return cudaErrorInvalidValue;
+        if (!make_map_3d(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, a.ab_bf16, KA, Rm, a.E, kBM))
+            return cudaErrorInvalidValue;
+    }
     if (!make_map_2d(&P.tmB, a.act_in, a.ab_bf16, KA, a.rows_in, 64)) return cudaErrorInvalidValue;
-    const size_t smem = tc_gemm_smem_bytes();
-    cudaError_t e = ensure_smem(tc_gemm_kernel, smem);
-    if (e != cudaSuccess) return e;
-    tc_gemm_kernel<<<num_sms, kThreads, smem, s>>>(P);
+    cudaError_t e;
+    if (a.quant) {
+        const size_t smem = kStages * kStageQ + sizeof(SmemTail) + 1024;
+        e = ensure_smem(tc_gemm_kernel<true>, smem);
+        if (e != cudaSuccess) return e;
+        tc_gemm_kernel<true><<<num_sms, kThreadsQ, smem, s>>>(P);
+    } else {
+        const size_t smem = kStages * kStage + sizeof(SmemTail) + 1024;
+        e = ensure_smem(tc_gemm_kernel<false>, smem);
+        if (e != cudaSuccess) return e;
+        tc_gemm_kernel<false><<<num_sms, kThreads, smem, s>>>(P);
+    }
     return cudaGetLastError();
 }
 

@@ -33,7 +33,7 @@ namespace tsmoe {
 
 namespace {
 
-constexpr int kNCW = 8;                       // consumer warps
+constexpr int kNCW = 16;                      // consumer warps
 constexpr int kThreads = (kNCW + 1) * 32;     // + one producer warp
 constexpr int kStageBytes = 24576;
 constexpr int kMaxStages = 6;
@@ -65,7 +65,7 @@ __host__ inline Plan make_plan(int fmt, int K, int tg_cap) {
         if (p.row_stride) p.row_stride = round_up(p.nb, 2) * 64 + 64;
     }
     p.xstride = round_up(2 * K, 128) + 64;
-    const size_t fixed = static_cast<size_t>(kNCW) * 2 * kRowTile * 8 * 4   // reduction
+    const size_t fixed = static_cast<size_t>(2) * kNCW * 2 * kRowTile * 8 * 4   // reduction x2
                          + static_cast<size_t>(nblk) * 8 * 4                  // INT4 x sums
                          + 8 * 4                                             // inverse prescale
                          + 2 * kMaxStages * 8                                // mbarriers
@@ -98,7 +98,7 @@ struct Carve {
     unsigned char* xs;
     float* xsum;      // [nblk][8]
     float* xinv;      // [8]
-    float* red;       // [kNCW][2][16][8]
+    float* red;       // [2 buffers][kNCW][2][16][8]
     uint64_t* full;   // [nstages]
     uint64_t* empty;  // [nstages]
     int* touched;     // [256]
@@ -114,7 +114,7 @@ __device__ inline Carve carve(unsigned char* base, const Plan& p, int K) {
     c.xs = q;                      q += static_cast<size_t>(p.tg) * p.xstride;
     c.xsum = reinterpret_cast<float*>(q);    q += static_cast<size_t>(K / kBlockK) * 8 * 4;
     c.xinv = reinterpret_cast<float*>(q);    q += 8 * 4;
-    c.red = reinterpret_cast<float*>(q);     q += kNCW * 2 * kRowTile * 8 * 4;
+    c.red = reinterpret_cast<float*>(q);     q += 2 * kNCW * 2 * kRowTile * 8 * 4;
     c.full = reinterpret_cast<uint64_t*>(q); q += kMaxStages * 8;
     c.empty = reinterpret_cast<uint64_t*>(q); q += kMaxStages * 8;
     c.touched = reinterpret_cast<int*>(q);   q += kMaxExperts * 4;
@@ -384,17 +384,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     const unsigned char* st = c.ring + static_cast<size_t>(s) * kStageBytes;
                     const unsigned char* xrow = c.xs + static_cast<size_t>(brow) * p.xstride + tid * 16;
                     float* ac = acc[m];
-                    for (int i = warp; i < nbc; i += kNCW) {
+                    auto block = [&](int i) {
                         const uint4 bx = *reinterpret_cast<const uint4*>(xrow + static_cast<size_t>(b0 + i) * 64);
                         if (FMT == FMT_MXFP4) {
                             const unsigned char* blk = st + static_cast<size_t>(i) * BB;
                             const uint2 cw = *reinterpret_cast<const uint2*>(blk + lane * 8);
                             const uint32_t sc = *reinterpret_cast<const uint16_t*>(blk + 256 + gid * 2);
+                            uint32_t pa[4], pb[4];
+                            e2m1x8_to_f16x2x4(cw.x, pa);
+                            e2m1x8_to_f16x2x4(cw.y, pb);
                             float d[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma_f16_16816(d, e2m1x2_to_f16x2(cw.x), e2m1x2_to_f16x2(cw.y),
-                                          e2m1x2_to_f16x2(cw.x >> 8), e2m1x2_to_f16x2(cw.y >> 8), bx.x, bx.y);
-                            mma_f16_16816(d, e2m1x2_to_f16x2(cw.x >> 16), e2m1x2_to_f16x2(cw.y >> 16),
-                                          e2m1x2_to_f16x2(cw.x >> 24), e2m1x2_to_f16x2(cw.y >> 24), bx.z, bx.w);
+                            mma_f16_16816(d, pa[0], pb[0], pa[1], pb[1], bx.x, bx.y);
+                            mma_f16_16816(d, pa[2], pb[2], pa[3], pb[3], bx.z, bx.w);
                             const float s0 = e8m0_to_float(sc & 0xFF), s1 = e8m0_to_float(sc >> 8);
                             ac[0] = fmaf(d[0], s0, ac[0]);
                             ac[1] = fmaf(d[1], s0, ac[1]);
@@ -422,15 +423,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                             const unsigned char* ra = st + static_cast<size_t>(gid) * p.row_stride + i * 64 + tid * 16;
                             const uint4 wa = *reinterpret_cast<const uint4*>(ra);
                             const uint4 wb = *reinterpret_cast<const uint4*>(ra + 8 * p.row_stride);
+                            float d[4] = {0.f, 0.f, 0.f, 0.f};
                             if (kMmaBf16) {
-                                mma_bf16_16816(ac, wa.x, wb.x, wa.y, wb.y, bx.x, bx.y);
-                                mma_bf16_16816(ac, wa.z, wb.z, wa.w, wb.w, bx.z, bx.w);
+                                mma_bf16_16816(d, wa.x, wb.x, wa.y, wb.y, bx.x, bx.y);
+                                mma_bf16_16816(d, wa.z, wb.z, wa.w, wb.w, bx.z, bx.w);
                             } else {
-                                mma_f16_16816(ac, wa.x, wb.x, wa.y, wb.y, bx.x, bx.y);
-                                mma_f16_16816(ac, wa.z, wb.z, wa.w, wb.w, bx.z, bx.w);
+                                mma_f16_16816(d, wa.x, wb.x, wa.y, wb.y, bx.x, bx.y);
+                                mma_f16_16816(d, wa.z, wb.z, wa.w, wb.w, bx.z, bx.w);
                             }
+                            ac[0] += d[0];
+                            ac[1] += d[1];
+                            ac[2] += d[2];
+                            ac[3] += d[3];
                         }
+                    };
+                    // two blocks in flight per warp: independent fragments, interleavable
+                    int i = warp;
+                    for (; i + kNCW < nbc; i += 2 * kNCW) {
+                        block(i);
+                        block(i + kNCW);
                     }
+                    if (i < nbc) block(i);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&c.empty[s]);
@@ -438,8 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
 
         // ---- cross-warp reduction (fixed order) + epilogue ------------------------------------
+        // two reduction buffers alternate between units: the barrier of unit u+1 proves every
+        // reader of unit u's buffer is done before unit u+2 overwrites it
+        float* redb = c.red + static_cast<size_t>(u & 1) * kNCW * 2 * kRowTile * 8;
         {
-            float* rw = c.red + static_cast<size_t>(warp) * 2 * kRowTile * 8;
+            float* rw = redb + static_cast<size_t>(warp) * 2 * kRowTile * 8;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 if (m >= nmat) break;
@@ -458,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 const int orow = rt * kRowTile + row;
                 float s0 = 0.0f, s1 = 0.0f;
                 for (int w = 0; w < kNCW; ++w) {
-                    s0 += c.red[(w * 2 + 0) * kRowTile * 8 + row * 8 + n];
-                    if (nmat == 2) s1 += c.red[(w * 2 + 1) * kRowTile * 8 + row * 8 + n];
+                    s0 += redb[(w * 2 + 0) * kRowTile * 8 + row * 8 + n];
+                    if (nmat == 2) s1 += redb[(w * 2 + 1) * kRowTile * 8 + row * 8 + n];
                 }
                 const float inv = c.xinv[n];
                 s0 *= inv;
@@ -475,7 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 }
             }
         }
-        named_bar(1, kNCW * 32);
     }
 }
 

@@ -13,7 +13,7 @@ enum { ACT_SILU = 0, ACT_GELU = 1, ACT_GPTOSS = 2 };
 enum { MODE_SOFTMAX_K = 0, MODE_SIGMOID_BIASED = 1, MODE_SOFTMAX_K_SCALED = 2 };
 
 // error codes written to the device status word (match ts_status)
-enum { DEV_ERR_INVALID = 1, DEV_ERR_TIMEOUT = 4 };
+enum { DEV_ERR_INVALID = 1, DEV_ERR_UNSUPPORTED = 2, DEV_ERR_TIMEOUT = 4 };
 
 constexpr int kMaxExperts = 256;
 constexpr int kRowTile = 16;   // rows per GEMV unit (the mma M)
@@ -102,11 +102,19 @@ struct GemmArgs {
     const int32_t* off;           // [E+1]
     const int32_t* perm;          // [T*k]
     int* status;
+    int quant;                    // 1: w0/w1 are packed MXFP4 (dequantised to f16 in smem)
+    size_t mat_bytes;             // packed bytes per expert matrix (quant)
+    const float* col_scale;       // quant: per route-list position, undoes the f16 prescale
+    unsigned* hmax;               // quant phase 0: per position max |h| (f32 bits, atomicMax)
 };
 cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
                                uint16_t* xs, cudaStream_t s);
 size_t tc_gemm_smem_bytes();
+cudaError_t launch_gather_rows_f16(const uint16_t* x, int adt, const int32_t* perm, int k, int H,
+                                   int n, uint16_t* xs, float* inv, unsigned* hmax, cudaStream_t s);
+cudaError_t launch_h_to_f16(const uint16_t* h, int adt, const unsigned* hmax, int I, int n,
+                            uint16_t* h16, float* inv, cudaStream_t s);
 
 cudaError_t launch_pack(int fmt, int nmat, int R, int K, const uint8_t* codes,
                         const uint8_t* scales, uint8_t* packed, cudaStream_t s);

@@ -19,7 +19,8 @@ namespace tsmoe {
 
 namespace {
 
-constexpr int kRouterWarps = 4;
+constexpr int kRouterWarps = 8;   // warps per token (experts are spread over them)
+
 
 // Order-preserving map of an f32 to u32 (larger float -> larger integer); -0 folds to +0 so
 // that equal keys tie and fall back to the expert id, as the f32 comparison does.
@@ -49,51 +50,76 @@ __device__ __forceinline__ float warp_dot_fixed(const float* a, LoadB loadb, int
     return warp_sum_xor(p);
 }
 
+// One CTA per token.  The experts' logits are spread over the CTA's warps; each warp keeps four
+// experts' lane chains in flight.  The summation order of every single logit is the fixed one
+// (lane l: fmaf over j, then the xor butterfly), so which warp computes it does not matter.
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_kernel(RouteArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(16) float xs[];     // [H] (only with x)
+    __shared__ float key[kMaxExperts];
+    __shared__ float sg[kMaxExperts];
+    __shared__ float ex[kMaxExperts];
+    __shared__ int sel[kMaxExperts];
+    __shared__ float rnorm;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kRouterWarps + warp;
+    const int t = blockIdx.x;
     const int E = a.E, H = a.H, k = a.k;
-    // per-warp smem: xs[H] f32 (only with x), key[E], sg[E], ex[k]
-    float* base = reinterpret_cast<float*>(smem_raw);
-    const int xs_len = a.x ? H : 0;
-    const int per_warp = xs_len + 2 * kMaxExperts + kMaxExperts;
-    float* xs = base + warp * per_warp;
-    float* key = xs + xs_len;
-    float* sg = key + kMaxExperts;
-    float* ex = sg + kMaxExperts;
-    __shared__ int sel_s[kRouterWarps][kMaxExperts];
     if (t >= a.T) return;
 
     // ---- step 1: optional RMSNorm + raw logits ------------------------------------------
     if (a.x) {
         const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * H;
-        for (int j = lane; j < H; j += 32) xs[j] = adt_bits_to_float(xr[j], a.adt);
+        for (int j = threadIdx.x; j < H; j += blockDim.x) xs[j] = adt_bits_to_float(xr[j], a.adt);
+        __syncthreads();
         if (a.rmsnorm) {
-            const float ss = warp_dot_fixed(xs, [&](int j) { return xs[j]; }, H, lane);
-            const float ms = __fdiv_rn(ss, static_cast<float>(H));
-            const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+            if (warp == 0) {
+                const float ss = warp_dot_fixed(xs, [&](int j) { return xs[j]; }, H, lane);
+                const float ms = __fdiv_rn(ss, static_cast<float>(H));
+                if (lane == 0) rnorm = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+            }
+            __syncthreads();
+            const float r = rnorm;
             uint16_t* xo = static_cast<uint16_t*>(a.xn_out) + static_cast<size_t>(t) * H;
-            for (int j = lane; j < H; j += 32) {
+            for (int j = threadIdx.x; j < H; j += blockDim.x) {
                 const uint16_t b = float_to_adt_bits(__fmul_rn(xs[j], r), a.adt);
                 xo[j] = b;
                 xs[j] = adt_bits_to_float(b, a.adt);
             }
+            __syncthreads();
         }
         const uint16_t* W = static_cast<const uint16_t*>(a.Wr);
-        for (int e = 0; e < E; ++e) {
-            const uint16_t* wr = W + static_cast<size_t>(e) * H;
-            const float l = warp_dot_fixed(xs, [&](int j) { return adt_bits_to_float(wr[j], a.adt); },
-                                           H, lane);
-            if (lane == 0) key[e] = l;   // raw logit for now
+        for (int e0 = warp * 4; e0 < E; e0 += kRouterWarps * 4) {
+            const int ne = min(4, E - e0);
+            const uint16_t* w0 = W + static_cast<size_t>(e0) * H;
+            const uint16_t* w1 = W + static_cast<size_t>(ne > 1 ? e0 + 1 : e0) * H;
+            const uint16_t* w2 = W + static_cast<size_t>(ne > 2 ? e0 + 2 : e0) * H;
+            const uint16_t* w3 = W + static_cast<size_t>(ne > 3 ? e0 + 3 : e0) * H;
+            float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+#pragma unroll 4
+            for (int j = lane; j < H; j += 32) {
+                const float xv = xs[j];
+                p0 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w0 + j), a.adt), p0);
+                p1 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w1 + j), a.adt), p1);
+                p2 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w2 + j), a.adt), p2);
+                p3 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w3 + j), a.adt), p3);
+            }
+            p0 = warp_sum_xor(p0);
+            p1 = warp_sum_xor(p1);
+            p2 = warp_sum_xor(p2);
+            p3 = warp_sum_xor(p3);
+            if (lane == 0) {
+                key[e0] = p0;
+                if (ne > 1) key[e0 + 1] = p1;
+                if (ne > 2) key[e0 + 2] = p2;
+                if (ne > 3) key[e0 + 3] = p3;
+            }
         }
-        __syncwarp();
     } else {
         const float* lr = a.logits_in + static_cast<size_t>(t) * E;
-        for (int e = lane; e < E; e += 32) key[e] = lr[e];
-        __syncwarp();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) key[e] = lr[e];
     }
+    __syncthreads();
+    if (warp != 0) return;
 
     // ---- step 2: keys per mode --------------------------------------------------------------
     for (int e = lane; e < E; e += 32) {
@@ -134,12 +160,11 @@ router_kernel(RouteArgs a) {
             for (int i = 0; i < kMaxExperts / 32; ++i)
                 if (lane + 32 * i == e) own[i] = 0ull;
         }
-        if (lane == 0) sel_s[warp][s] = e;
+        if (lane == 0) sel[s] = e;
     }
     __syncwarp();
 
     // ---- weights ------------------------------------------------------------------------------
-    const int* sel = sel_s[warp];
     if (a.mode == MODE_SIGMOID_BIASED) {
         for (int s = lane; s < k; s += 32) ex[s] = sg[sel[s]];
     } else {
@@ -225,14 +250,12 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
 
 cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
-    const int xs_len = a.x ? a.H : 0;
-    const size_t smem = static_cast<size_t>(kRouterWarps) * (xs_len + 3 * kMaxExperts) * 4;
-    if (smem > 48 * 1024) {
+    const size_t smem = a.x ? static_cast<size_t>(a.H) * 4 : 0;
+    if (smem > 40 * 1024) {
         cudaError_t e = ensure_smem(router_kernel, smem);
         if (e != cudaSuccess) return e;
     }
-    const int grid = (a.T + kRouterWarps - 1) / kRouterWarps;
-    router_kernel<<<grid, kRouterWarps * 32, smem, s>>>(a);
+    router_kernel<<<a.T, kRouterWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 

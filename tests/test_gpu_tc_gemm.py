@@ -32,6 +32,9 @@ CASES = [
     (5, 300, dict(H=256, I=256, E=4, k=2)),           # > 256 routes per expert: 2+ route tiles
     (1, 20, dict(H=128, I=256, E=8, k=2)),            # f16 weights + f16 activations
     (5, 2048, None),                                  # full Mixtral-8x7B prefill chunk
+    (2, 40, dict(H=512, I=384, E=8, k=4)),            # MXFP4 + clamped SwiGLU + biases
+    (3, 77, dict(H=640, I=448, E=8, k=4)),            # MXFP4, skewed, partial 128-row blocks
+    (3, 512, None),                                   # full gpt-oss prefill micro-batch
 ]
 
 
@@ -68,7 +71,8 @@ def test_tc_gemm_parity(case):
                   oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"])
 
 
-@pytest.mark.parametrize("case", [(5, 8, dict(H=512, I=1024, E=8, k=2)), (5, 64, dict(H=256, I=512, E=8, k=2))],
+@pytest.mark.parametrize("case", [(5, 8, dict(H=512, I=1024, E=8, k=2)), (5, 64, dict(H=256, I=512, E=8, k=2)),
+                                  (2, 8, dict(H=2880, I=2880, E=32, k=4)), (3, 48, dict(H=512, I=512, E=8, k=4))],
                          ids=_ids)
 def test_gemm_and_gemv_paths_agree(case):
     moe = _moe()
@@ -76,7 +80,7 @@ def test_gemm_and_gemv_paths_agree(case):
     L, D = _make(cfg, T, shapes)
     c = L["cfg"]
     ex, _ = gpu_layer(D)
-    idx, w, _, _ = moe.router_route(D["x"], D["Wr"], c["k"])
+    idx, w, _, _ = moe.router_route(D["x"], D["Wr"], c["k"], router_bias=D["router_bias"])
     ya, ya32 = moe.forward(D["x"], ex, idx, w, want_f32=True, path="gemv")
     yb, yb32 = moe.forward(D["x"], ex, idx, w, want_f32=True, path="gemm")
     torch.cuda.synchronize()
@@ -96,11 +100,12 @@ def test_tc_gemm_deterministic():
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
 
 
-def test_gemm_path_refuses_quantised_weights():
+def test_gemm_path_refuses_int4_weights():
     moe = _moe()
-    L, D = _make(2, 16, dict(H=256, I=256, E=8, k=4))
+    L, D = _make(4, 16, dict(H=256, I=128, E=8, k=4, shared_I=64))
     ex, _ = gpu_layer(D)
-    idx, w, _, _ = moe.router_route(D["x"], D["Wr"], 4, router_bias=D["router_bias"])
+    idx, w, _, _ = moe.router_route(D["x"], D["Wr"], 4, mode="softmax_k_scaled",
+                                    per_expert_scale=D["scale"])
     with pytest.raises(moe.TsMoeError) as ei:
         moe.forward(D["x"], ex, idx, w, path="gemm")
     assert ei.value.status == 2
