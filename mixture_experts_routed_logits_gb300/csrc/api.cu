@@ -210,6 +210,7 @@ ts_status ts_moe_router_route(const void* x, int32_t adt, int32_t T, int32_t H, 
     if (H > 12288) return fail(TS_ERR_UNSUPPORTED, "%s: H=%d above 12288", what, H);
     if (rmsnorm != 0 && rmsnorm != 1) return fail(TS_ERR_INVALID_ARG, "%s: rmsnorm must be 0 or 1", what);
     if (T > 0 && (!x || !W_r)) return fail(TS_ERR_INVALID_ARG, "%s: x or W_r is NULL", what);
+    if (!aligned(W_r, 16)) return fail(TS_ERR_INVALID_ARG, "%s: W_r must be 16-byte aligned", what);
     if (T > 0 && rmsnorm && !xn_out) return fail(TS_ERR_INVALID_ARG, "%s: rmsnorm needs xn_out", what);
     if (!(eps >= 0.0f)) return fail(TS_ERR_INVALID_ARG, "%s: eps must be >= 0", what);
     RouteArgs a{};

@@ -330,7 +330,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         const int gid = lane >> 2, tid = lane & 3;
         int it = 0;
         bool bad_scale = false;
+        const int RTm = R / kRowTile;               // 16-row tiles that exist per matrix
         for (int i = blockIdx.x; i < items && !tl->abort_flag; i += gridDim.x) {
+            int j, mb, tile_i;
+            decode(i, j, mb, tile_i);
+            const int rt0 = (mb * rows_per_item) / kRowTile;
+            const int rt1 = a.phase == 0 ? rt0 : rt0 + kBM / kRowTile;
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int s = it % kStages;
                 if (!mbar_wait_bounded(&tl->full[s], (it / kStages) & 1)) {
@@ -345,6 +350,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll 2
                 for (int qb = dw; qb < 32; qb += kDqWarps) {
                     const int tile = qb >> 4, rt = (qb >> 1) & 7, bb = qb & 1;
+                    // row tiles past the matrix were not copied: their A rows only feed output
+                    // rows that are never stored, so they are left as they are
+                    if ((tile == 0 ? rt0 : rt1) + rt >= RTm) continue;
                     const unsigned char* blk = stg + (tile * 8 + rt) * 2 * kPackBlk + bb * kPackBlk;
                     const uint2 cw = *reinterpret_cast<const uint2*>(blk + lane * 8);
                     const uint32_t sc = *reinterpret_cast<const uint16_t*>(blk + 256 + gid * 2);

@@ -50,17 +50,40 @@ __device__ __forceinline__ float warp_dot_fixed(const float* a, LoadB loadb, int
     return warp_sum_xor(p);
 }
 
-// One CTA per token.  The experts' logits are spread over the CTA's warps; each warp keeps four
-// experts' lane chains in flight.  The summation order of every single logit is the fixed one
-// (lane l: fmaf over j, then the xor butterfly), so which warp computes it does not matter.
+// One CTA per token.  The router weights stream through shared memory in stages of `rb` rows
+// (one 1-D bulk copy per stage, up to `ns` stages in flight, mbarrier completion); warp w
+// computes the logit of row w of each stage.  The summation order of every logit is the fixed
+// one (lane l: fmaf over j, then the xor butterfly), so which warp computes it does not matter.
+struct RouterPlan {
+    int rb, ns;           // rows per stage, stages in flight
+    size_t smem;
+};
+
+__host__ inline RouterPlan router_plan(int H, int has_x) {
+    RouterPlan p{8, 3, 0};
+    if (!has_x) return p;
+    const size_t budget = 200 * 1024;
+    const size_t xs = static_cast<size_t>(H) * 4;
+    while (p.rb > 1 || p.ns > 1) {
+        const size_t need = xs + static_cast<size_t>(p.ns) * p.rb * H * 2 + 64;
+        if (need <= budget) break;
+        if (p.ns > 1) --p.ns; else p.rb /= 2;
+    }
+    p.smem = xs + static_cast<size_t>(p.ns) * p.rb * H * 2 + 64;
+    return p;
+}
+
 __global__ void __launch_bounds__(kRouterWarps * 32)
-router_kernel(RouteArgs a) {
-    extern __shared__ __align__(16) float xs[];     // [H] (only with x)
+router_kernel(RouteArgs a, int rb, int ns) {
+    extern __shared__ __align__(128) unsigned char rsm[];
     __shared__ float key[kMaxExperts];
     __shared__ float sg[kMaxExperts];
     __shared__ float ex[kMaxExperts];
     __shared__ int sel[kMaxExperts];
     __shared__ float rnorm;
+    __shared__ __align__(8) uint64_t full[3];
+    __shared__ __align__(8) uint64_t empty[3];
+    __shared__ volatile int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     const int E = a.E, H = a.H, k = a.k;
@@ -68,6 +91,30 @@ router_kernel(RouteArgs a) {
 
     // ---- step 1: optional RMSNorm + raw logits ------------------------------------------
     if (a.x) {
+        float* xs = reinterpret_cast<float*>(rsm);
+        uint16_t* wst = reinterpret_cast<uint16_t*>(rsm + static_cast<size_t>(H) * 4);
+        const size_t stage_elems = static_cast<size_t>(rb) * H;
+        const int nst = (E + rb - 1) / rb;
+        const uint16_t* W = static_cast<const uint16_t*>(a.Wr);
+        if (threadIdx.x == 0) {
+            abort_flag = 0;
+            for (int q = 0; q < ns; ++q) {
+                mbar_init(&full[q], 1);
+                mbar_init(&empty[q], kRouterWarps);
+            }
+            fence_mbar_init();
+        }
+        __syncthreads();
+        auto issue = [&](int st) {
+            const int e0 = st * rb;
+            const int rows = min(rb, E - e0);
+            const uint32_t bytes = static_cast<uint32_t>(rows) * H * 2;
+            const int slot = st % ns;
+            mbar_arrive_expect_tx(&full[slot], bytes);
+            bulk_g2s(wst + slot * stage_elems, W + static_cast<size_t>(e0) * H, bytes, &full[slot]);
+        };
+        if (threadIdx.x == 0)
+            for (int st = 0; st < min(ns, nst); ++st) issue(st);
         const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * H;
         for (int j = threadIdx.x; j < H; j += blockDim.x) xs[j] = adt_bits_to_float(xr[j], a.adt);
         __syncthreads();
@@ -87,33 +134,29 @@ router_kernel(RouteArgs a) {
             }
             __syncthreads();
         }
-        const uint16_t* W = static_cast<const uint16_t*>(a.Wr);
-        for (int e0 = warp * 4; e0 < E; e0 += kRouterWarps * 4) {
-            const int ne = min(4, E - e0);
-            const uint16_t* w0 = W + static_cast<size_t>(e0) * H;
-            const uint16_t* w1 = W + static_cast<size_t>(ne > 1 ? e0 + 1 : e0) * H;
-            const uint16_t* w2 = W + static_cast<size_t>(ne > 2 ? e0 + 2 : e0) * H;
-            const uint16_t* w3 = W + static_cast<size_t>(ne > 3 ? e0 + 3 : e0) * H;
-            float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
-#pragma unroll 4
-            for (int j = lane; j < H; j += 32) {
-                const float xv = xs[j];
-                p0 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w0 + j), a.adt), p0);
-                p1 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w1 + j), a.adt), p1);
-                p2 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w2 + j), a.adt), p2);
-                p3 = __fmaf_rn(xv, adt_bits_to_float(__ldg(w3 + j), a.adt), p3);
+        for (int st = 0; st < nst; ++st) {
+            const int slot = st % ns;
+            const bool ok = !abort_flag && mbar_wait_bounded(&full[slot], (st / ns) & 1);
+            if (!ok) {
+                if (lane == 0) abort_flag = 1;
+            } else if (warp < rb && st * rb + warp < E) {
+                const uint16_t* wr = wst + slot * stage_elems + static_cast<size_t>(warp) * H;
+                const float l = warp_dot_fixed(xs, [&](int j) { return adt_bits_to_float(wr[j], a.adt); },
+                                               H, lane);
+                if (lane == 0) key[st * rb + warp] = l;
             }
-            p0 = warp_sum_xor(p0);
-            p1 = warp_sum_xor(p1);
-            p2 = warp_sum_xor(p2);
-            p3 = warp_sum_xor(p3);
-            if (lane == 0) {
-                key[e0] = p0;
-                if (ne > 1) key[e0 + 1] = p1;
-                if (ne > 2) key[e0 + 2] = p2;
-                if (ne > 3) key[e0 + 3] = p3;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (threadIdx.x == 0 && st + ns < nst && !abort_flag) {
+                // the slot is refilled once every warp has read it
+                if (mbar_wait_bounded(&empty[slot], (st / ns) & 1)) issue(st + ns);
+                else abort_flag = 1;
             }
         }
+        // no copy may still be in flight when the CTA exits
+        if (threadIdx.x == 0)
+            for (int st = max(0, nst - ns); st < nst; ++st)
+                mbar_wait_bounded(&full[st % ns], (st / ns) & 1);
     } else {
         const float* lr = a.logits_in + static_cast<size_t>(t) * E;
         for (int e = threadIdx.x; e < E; e += blockDim.x) key[e] = lr[e];
@@ -176,10 +219,11 @@ router_kernel(RouteArgs a) {
     if (lane == 0)
         for (int s = 0; s < k; ++s) sum = __fadd_rn(sum, ex[s]);   // slot order
     sum = __shfl_sync(0xffffffffu, sum, 0);
+    const bool aborted = a.x && abort_flag;
     for (int s = lane; s < k; s += 32) {
         float wv = __fdiv_rn(ex[s], sum);
         if (a.mode == MODE_SOFTMAX_K_SCALED) wv = __fmul_rn(wv, a.scale[sel[s]]);
-        a.idx[static_cast<size_t>(t) * k + s] = sel[s];
+        a.idx[static_cast<size_t>(t) * k + s] = aborted ? -1 : sel[s];   // -1: the wait gave up
         a.w[static_cast<size_t>(t) * k + s] = wv;
     }
 }
@@ -250,12 +294,12 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
 
 cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
-    const size_t smem = a.x ? static_cast<size_t>(a.H) * 4 : 0;
-    if (smem > 40 * 1024) {
-        cudaError_t e = ensure_smem(router_kernel, smem);
+    const RouterPlan p = router_plan(a.H, a.x != nullptr);
+    if (p.smem > 40 * 1024) {
+        cudaError_t e = ensure_smem(router_kernel, p.smem);
         if (e != cudaSuccess) return e;
     }
-    router_kernel<<<a.T, kRouterWarps * 32, smem, s>>>(a);
+    router_kernel<<<a.T, kRouterWarps * 32, p.smem, s>>>(a, p.rb, p.ns);
     return cudaGetLastError();
 }
 
