@@ -210,6 +210,25 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
                               const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
                               size_t ws_bytes, int32_t path, void* stream);
 
+/* As ts_moe_forward (automatic path), for callers that cannot allocate device memory: instead
+ * of a caller-provided workspace it uses a scratch array that lives in the library's own device
+ * memory (16 MiB per GPU, held until the process exits).  The source pages have no counterpart;
+ * it exists because some callers own all device memory themselves or must not allocate while
+ * they run.  It calls no allocator (no cudaMalloc, no cudaFree).
+ *   - Calls that need more scratch than 16 MiB (ts_moe_workspace_size) return
+ *     TS_ERR_WORKSPACE and launch nothing.
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *   - Every call on a device shares the one scratch array and it keeps the last call's
+ *     contents; the call clears what must start at zero (the device status word) itself.
+ *     Calls that overlap on the GPU (different streams, no ordering between them) race on the
+ *     scratch and produce wrong results: order them on one stream or use ts_moe_forward.
+ * Other arguments as ts_moe_forward.                                                        */
+ts_status ts_moe_forward_noalloc(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
+                                 const int32_t* idx, const float* w, int32_t k,
+                                 const ts_moe_experts* shared, void* y, float* y_f32,
+                                 void* stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* Diagnostics.                                                                                */
 /* ------------------------------------------------------------------------------------------ */

@@ -72,6 +72,8 @@ def lib():
             "ts_moe_forward_path": ([vp, i32, i32, pe, vp, vp, i32, pe, vp, vp, vp, sz, i32, vp],
                                     ctypes.c_int),
             "ts_moe_device_status": ([vp, ctypes.POINTER(i32), vp], ctypes.c_int),
+            "ts_moe_forward_noalloc": ([vp, i32, i32, pe, vp, vp, i32, pe, vp, vp, vp],
+                                       ctypes.c_int),
             "ts_moe_set_phase_events": ([ctypes.POINTER(vp), i32], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
@@ -230,6 +232,26 @@ def forward(x, ex: Experts, idx, w, shared: Experts | None = None, want_f32=Fals
                                     k, None if shared is None else ctypes.byref(shared.c),
                                     _ptr(y), _ptr(y32), _ptr(ws), ws.numel(), PATH[path],
                                     _stream(stream)))
+    return y, y32
+
+
+def forward_noalloc(x, ex: Experts, idx, w, shared: Experts | None = None, want_f32=False,
+                    out=None, stream=None):
+    """forward() without a workspace: the library's static device scratch is used (see
+    ts_moe_forward_noalloc in include/ts_moe.h for its size limit and sharing rules)."""
+    import torch
+    T, H = x.shape
+    k = idx.shape[1]
+    adt = {torch.float16: "f16", torch.bfloat16: "bf16"}[x.dtype]
+    if out is None:
+        y = torch.empty_like(x)
+        y32 = torch.empty((T, H), dtype=torch.float32, device=x.device) if want_f32 else None
+    else:
+        y, y32 = out
+    check(lib().ts_moe_forward_noalloc(_ptr(x), ADT[adt], T, ctypes.byref(ex.c), _ptr(idx),
+                                       _ptr(w), k,
+                                       None if shared is None else ctypes.byref(shared.c),
+                                       _ptr(y), _ptr(y32), _stream(stream)))
     return y, y32
 
 

@@ -132,6 +132,14 @@ ts_status launch_gemv_checked(const GemvArgs& a, cudaStream_t st, const char* wh
 
 }  // namespace
 
+namespace tsmoe {
+// Lets other translation units of the library record a ts_last_error() message.
+int record_error_code(int status, const char* msg) {
+    g_err = msg;
+    return status;
+}
+}  // namespace tsmoe
+
 extern "C" {
 
 const char* ts_last_error(void) { return g_err.c_str(); }

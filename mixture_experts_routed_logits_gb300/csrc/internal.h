@@ -116,6 +116,9 @@ cudaError_t launch_gather_rows_f16(const uint16_t* x, int adt, const int32_t* pe
 cudaError_t launch_h_to_f16(const uint16_t* h, int adt, const unsigned* hmax, int I, int n,
                             uint16_t* h16, float* inv, cudaStream_t s);
 
+// records the thread's ts_last_error() message (defined in api.cu); returns `status`
+int record_error_code(int status, const char* msg);
+
 cudaError_t launch_pack(int fmt, int nmat, int R, int K, const uint8_t* codes,
                         const uint8_t* scales, uint8_t* packed, cudaStream_t s);
 
