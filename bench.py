@@ -286,9 +286,14 @@ def main():
     torch.cuda.synchronize()
 
     flush = synth.make_l2_flush("cuda")
-    gemm_path = T > 8 and cfg["fmt"] in ("bf16", "f16") and H % 64 == 0 and I % 64 == 0
-    # router, route list, [gather], phase 1, phase 2, combine (+ 2 shared-expert GEMVs)
-    n_launch_step = 5 + (1 if gemm_path else 0) + (2 if cfg.get("shared_I") else 0)
+    # the library's automatic choice: tensor-core grouped GEMM above 8 tokens for MXFP4 and for
+    # 16-bit weights of the activation type (H, I multiples of 64), else the streaming GEMV
+    gemm_path = (T > 8 and H % 64 == 0 and I % 64 == 0
+                 and (cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"]))
+    # GEMV decode (T*k <= 512): router, phase 1, phase 2 (+ fused route list and combine);
+    # otherwise router, route list, [gather], phase 1, phase 2, combine; + 2 shared-expert GEMVs
+    fused_decode = (not gemm_path) and T * k <= 512
+    n_launch_step = (3 if fused_decode else 5 + (1 if gemm_path else 0)) + (2 if cfg.get("shared_I") else 0)
 
     def timed(K):
         b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -332,7 +337,10 @@ def main():
     # ---- per-phase breakdown: graphs carrying event-record nodes after every launch ----------------
     # event order in a step: 6 router, 0 route list, 1 phase 1, [2 shared phase 1], 3 phase 2,
     # [4 shared phase 2], 5 combine
-    order = [6, 0, 1] + ([2] if cfg.get("shared_I") else []) + [3] + ([4] if cfg.get("shared_I") else []) + [5]
+    if gemm_path:
+        order = [6, 0, 1, 3, 5]
+    else:   # GEMV: routed phase 1, shared phase 1, shared phase 2, routed phase 2 (+ combine)
+        order = [6, 0, 1] + ([2, 4] if cfg.get("shared_I") else []) + [3, 5]
     samples = {moe.PHASES[j]: [] for j in order}
     for i in range(3 if args.profile else min(args.steps, 50)):
         flush.zero_()
@@ -367,7 +375,7 @@ def main():
     routes = T * k
     p1_flop = 2.0 * routes * 2 * I * H
     p2_flop = 2.0 * routes * H * I
-    if gemm_path:
+    if gemm_path and fmt != "mxfp4":
         # tensor-bound: FLOPs of the phase-1 grouped GEMM over its launch time, against the
         # sustained bf16 peak (the kernel runs inside a seconds-long loop)
         achieved = p1_flop / (p1_ms * 1e-3) / 1e12
@@ -378,7 +386,9 @@ def main():
         step_tf = (p1_flop + p2_flop) / (ms_max * 1e-3) / 1e12
     else:
         achieved = p1_bytes / (p1_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": "experts_phase1 (gate/up GEMV)",
+        roof = {"bound": "hbm",
+                "kernel": ("experts_phase1 (tcgen05 grouped GEMM over packed MXFP4, gate/up)"
+                           if gemm_path else "experts_phase1 (gate/up GEMV)"),
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_source": peak_src,
                 "traffic": None, "algorithmic_bytes": p1_bytes, "launch_ms": p1_ms}

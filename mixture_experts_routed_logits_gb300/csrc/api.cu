@@ -89,7 +89,7 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
 }
 
 struct WsLayout {
-    size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hmax, hinv, h16, total;
+    size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hmax, hinv, h16, cmb, total;
 };
 
 WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts* sh) {
@@ -112,6 +112,7 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
         L.s = take(static_cast<size_t>(T) * ex->H * 4);
     }
     L.xs = take(Tk * ex->H * 2);   // activations in route-list order (tensor-core path)
+    L.cmb = take(static_cast<size_t>(ex->H / kRowTile) * 4);   // fused-combine counters
     if (ex->fmt == FMT_MXFP4) {      // f16 operands of the MXFP4 tensor-core path
         L.xinv = take(Tk * 4);
         L.hmax = take(Tk * 4);
@@ -309,7 +310,9 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     int32_t* perm = reinterpret_cast<int32_t*>(W + L.perm);
     int32_t* inv = reinterpret_cast<int32_t*>(W + L.inv);
 
-    cudaError_t e = launch_build_routes(idx, T, ex->E, k, off, perm, inv, status, st);
+    cudaError_t e = cudaSuccess;
+    if (use_gemm || static_cast<long long>(T) * k > 512)   // else built inside the GEMV kernels
+        e = launch_build_routes(idx, T, ex->E, k, off, perm, inv, status, st);
     if (e == cudaSuccess) e = phase_mark(0, st);
     if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: route list");
 
@@ -379,6 +382,11 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: tensor-core phase 2");
     }
 
+    // Decode-sized GEMV calls build the route list inside the expert kernels and fuse the
+    // combine into phase 2 (fewer launches); the order is routed phase 1, shared phase 1,
+    // shared phase 2 (the combine's seed), routed phase 2 (+ combine).
+    const bool fused = !use_gemm && static_cast<long long>(T) * k <= 512;
+    int* cmb = reinterpret_cast<int*>(W + L.cmb);
     GemvArgs g{};
     g.act = ex->act;
     g.limit = ex->swiglu_limit;
@@ -388,7 +396,6 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     g.k = k;
     g.E = ex->E;
     g.status = status;
-    // phase 1: gate/up + activation -> h (16-bit, by route id)
     g.fmt = ex->fmt;
     g.phase = 0;
     g.w0 = static_cast<const uint8_t*>(ex->gate);
@@ -400,9 +407,13 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     g.mat_bytes = matrix_bytes(ex->fmt, ex->I, ex->H);
     g.in = static_cast<const uint16_t*>(x);
     g.out = W + L.h;
-    g.off = off;
-    g.perm = perm;
+    g.off = fused ? nullptr : off;
+    g.perm = fused ? nullptr : perm;
+    g.idx = fused ? idx : nullptr;
     g.dense = 0;
+    g.cmb_mode = fused ? 1 : 0;
+    g.cmb_cnt = cmb;
+    g.cmb_n = ex->H / kRowTile;
     if (!use_gemm) {
         if ((s = launch_gemv_checked(g, st, "ts_moe_forward: expert phase 1")) != TS_OK) return s;
         if ((e = phase_mark(1, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
@@ -424,27 +435,12 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         gs.out = W + L.hs;
         gs.off = nullptr;
         gs.perm = nullptr;
+        gs.idx = nullptr;
         gs.dense = 1;
         gs.k = 1;
+        gs.cmb_mode = 0;
         if ((s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 1")) != TS_OK) return s;
         if ((e = phase_mark(2, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
-    }
-    // phase 2: down projection -> e (f32, by route id)
-    g.phase = 1;
-    g.w0 = static_cast<const uint8_t*>(ex->down);
-    g.w1 = nullptr;
-    g.b0 = static_cast<const uint16_t*>(ex->down_b);
-    g.b1 = nullptr;
-    g.R = ex->H;
-    g.K = ex->I;
-    g.mat_bytes = matrix_bytes(ex->fmt, ex->H, ex->I);
-    g.in = reinterpret_cast<const uint16_t*>(W + L.h);
-    g.out = W + L.e;
-    if (!use_gemm) {
-        if ((s = launch_gemv_checked(g, st, "ts_moe_forward: expert phase 2")) != TS_OK) return s;
-        if ((e = phase_mark(3, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
-    }
-    if (shared) {
         gs.phase = 1;
         gs.w0 = static_cast<const uint8_t*>(shared->down);
         gs.w1 = nullptr;
@@ -458,19 +454,41 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         if ((s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 2")) != TS_OK) return s;
         if ((e = phase_mark(4, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
     }
-    CombineArgs c{};
-    c.e = reinterpret_cast<const float*>(W + L.e);
-    c.w = w;
-    c.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
-    c.y = y;
-    c.y_f32 = y_f32;
-    c.T = T;
-    c.H = ex->H;
-    c.k = k;
-    c.adt = adt;
-    e = launch_combine(c, st);
-    if (e == cudaSuccess) e = phase_mark(5, st);
-    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: combine");
+    // phase 2: down projection -> e (f32, by route id)
+    g.phase = 1;
+    g.w0 = static_cast<const uint8_t*>(ex->down);
+    g.w1 = nullptr;
+    g.b0 = static_cast<const uint16_t*>(ex->down_b);
+    g.b1 = nullptr;
+    g.R = ex->H;
+    g.K = ex->I;
+    g.mat_bytes = matrix_bytes(ex->fmt, ex->H, ex->I);
+    g.in = reinterpret_cast<const uint16_t*>(W + L.h);
+    g.out = W + L.e;
+    g.cmb_mode = fused ? 2 : 0;
+    g.w = w;
+    g.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
+    g.y = y;
+    g.y_f32 = y_f32;
+    if (!use_gemm) {
+        if ((s = launch_gemv_checked(g, st, "ts_moe_forward: expert phase 2")) != TS_OK) return s;
+        if ((e = phase_mark(3, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
+    }
+    if (!fused) {
+        CombineArgs c{};
+        c.e = reinterpret_cast<const float*>(W + L.e);
+        c.w = w;
+        c.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
+        c.y = y;
+        c.y_f32 = y_f32;
+        c.T = T;
+        c.H = ex->H;
+        c.k = k;
+        c.adt = adt;
+        e = launch_combine(c, st);
+        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: combine");
+    }
+    if ((e = phase_mark(5, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
     return TS_OK;
 }
 

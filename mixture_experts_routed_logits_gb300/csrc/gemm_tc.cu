@@ -238,11 +238,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 const int r1 = a.phase == 0 ? r0 : r0 + kBM;
                 const int RT = R / kRowTile;                // 16-row tiles per expert matrix
                 const int nblk = K / kBlockK;
-                int nq = 0;                                 // packed row tiles copied per stage
-                if (QUANT) {
-                    for (int t = 0; t < 8; ++t) nq += (r0 / kRowTile + t < RT) + (r1 / kRowTile + t < RT);
-                }
-                const uint32_t bytes = (QUANT ? nq * 2 * kPackBlk : 2 * kATile) + nbox * kBBox;
+                (void)RT;
+                (void)nblk;
+                const uint32_t bytes = (QUANT ? 2 * 8 * 2 * kPackBlk : 2 * kATile) + nbox * kBBox;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait_bounded(&tl->empty[s], ((it / kStages) & 1) ^ 1)) {
@@ -253,21 +251,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     unsigned char* st = base + s * SB;
                     mbar_arrive_expect_tx(&tl->full[s], bytes);
                     if (QUANT) {
+                        // one TMA per matrix: 8 packed 16-row tiles x 2 blocks (4352 bytes); row
+                        // tiles past the matrix come back zero-filled
                         unsigned char* stg = st + kStage;
-                        const uint8_t* m0 = static_cast<const uint8_t*>(a.w0) + static_cast<size_t>(e) * a.mat_bytes;
-                        const uint8_t* m1 = static_cast<const uint8_t*>(a.phase == 0 ? a.w1 : a.w0) +
-                                            static_cast<size_t>(e) * a.mat_bytes;
-                        for (int t = 0; t < 8; ++t) {
-                            const int rta = r0 / kRowTile + t, rtb = r1 / kRowTile + t;
-                            if (rta < RT)
-                                bulk_g2s(stg + t * 2 * kPackBlk,
-                                         m0 + (static_cast<size_t>(rta) * nblk + 2 * kb) * kPackBlk,
-                                         2 * kPackBlk, &tl->full[s]);
-                            if (rtb < RT)
-                                bulk_g2s(stg + (8 + t) * 2 * kPackBlk,
-                                         m1 + (static_cast<size_t>(rtb) * nblk + 2 * kb) * kPackBlk,
-                                         2 * kPackBlk, &tl->full[s]);
-                        }
+                        tma_load_3d(stg, &P.tmA0, 2 * kb * (kPackBlk / 4), r0 / kRowTile, e, &tl->full[s]);
+                        tma_load_3d(stg + 8 * 2 * kPackBlk, a.phase == 0 ? &P.tmA1 : &P.tmA0,
+                                    2 * kb * (kPackBlk / 4), r1 / kRowTile, e, &tl->full[s]);
                     } else {
                         tma_load_3d(st, &P.tmA0, kb * kBK, r0, e, &tl->full[s]);
                         tma_load_3d(st + kATile, a.phase == 0 ? &P.tmA1 : &P.tmA0, kb * kBK, r1, e,
@@ -419,9 +408,11 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     float g[16], u[16];
                     tmem_ld16(tq + c0, g);
                     tmem_ld16(tq + 256 + c0, u);
+                    unsigned hm[16];
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         const int c = c0 + t;
+                        hm[t] = 0u;
                         if (vr && c < n_valid) {
                             float gv = g[t], uv = u[t];
                             if (QUANT) {
@@ -432,8 +423,16 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                             const float h = act_fn(a.act, gv + bg, uv + bu, a.limit, a.alpha);
                             const uint16_t hb = float_to_adt_bits(h, a.adt);
                             hout[static_cast<size_t>(p0 + c) * R + row] = hb;
-                            if (QUANT)
-                                atomicMax(a.hmax + p0 + c, __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt))));
+                            if (QUANT) hm[t] = __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt)));
+                        }
+                    }
+                    if (QUANT) {
+                        // per-route max |h| (positive floats order like their bit patterns):
+                        // reduced over the warp's 32 rows first, one atomic per warp and column
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const unsigned mv = __reduce_max_sync(0xffffffffu, hm[t]);
+                            if (lane == 0 && c0 + t < n_valid) atomicMax(a.hmax + p0 + c0 + t, mv);
                         }
                     }
                 }
@@ -574,6 +573,21 @@ bool make_map_3d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed MXFP4 matrices [E][R/16 tiles][K/32 blocks x 272 B] as a 3-D uint32 tensor
+// {68 * nblk, R/16, E}; a {136, 8, 1} box is 8 row tiles x 2 blocks (one 64-column stage).
+bool make_map_packed(CUtensorMap* m, const void* base, uint64_t K, uint64_t R, uint64_t E) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t nblk = K / kBlockK;
+    const cuuint64_t dims[3] = {nblk * (kPackBlk / 4), R / kRowTile, E};
+    const cuuint64_t strides[2] = {nblk * kPackBlk, (R / kRowTile) * nblk * kPackBlk};
+    const cuuint32_t box[3] = {2 * (kPackBlk / 4), 8, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_2d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint64_t rows,
                  uint32_t box_rows) {
     auto fn = encode_fn();
@@ -622,6 +636,10 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     if (!a.quant) {
         if (!make_map_3d(&P.tmA0, a.w0, a.ab_bf16, KA, Rm, a.E, kBM)) return cudaErrorInvalidValue;
         if (!make_map_3d(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, a.ab_bf16, KA, Rm, a.E, kBM))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_map_packed(&P.tmA0, a.w0, KA, Rm, a.E)) return cudaErrorInvalidValue;
+        if (!make_map_packed(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, KA, Rm, a.E))
             return cudaErrorInvalidValue;
     }
     if (!make_map_2d(&P.tmB, a.act_in, a.ab_bf16, KA, a.rows_in, 64)) return cudaErrorInvalidValue;

@@ -34,7 +34,8 @@ namespace tsmoe {
 namespace {
 
 constexpr int kNCW = 16;                      // consumer warps
-constexpr int kThreads = (kNCW + 1) * 32;     // + one producer warp
+constexpr int kThreads = (kNCW + 2) * 32;     // + one producer warp + one reducer warp
+constexpr int kMaxLocalRoutes = 512;          // route lists built inside the kernel up to this
 constexpr int kStageBytes = 24576;
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 225 * 1024;
@@ -69,7 +70,10 @@ __host__ inline Plan make_plan(int fmt, int K, int tg_cap) {
                          + static_cast<size_t>(nblk) * 8 * 4                  // INT4 x sums
                          + 8 * 4                                             // inverse prescale
                          + 2 * kMaxStages * 8                                // mbarriers
-                         + (3 * kMaxExperts + 1 + 8) * 4;                    // unit tables
+                         + (3 * kMaxExperts + 1 + 8) * 4                     // unit tables
+                         + 2 * 8 * 4 + 4 * 8                                 // reducer hand-off
+                         + (kMaxExperts + 1 + kMaxLocalRoutes) * 4            // in-kernel routes
+                         + 16 * 16;                                           // region padding
     for (int ns = kMaxStages; ns >= 2; --ns) {
         const size_t ring = static_cast<size_t>(ns) * kStageBytes;
         if (ring + fixed >= static_cast<size_t>(kSmemBudget)) continue;
@@ -105,22 +109,38 @@ struct Carve {
     int* cnt;         // [256]
     int* goff;        // [257]
     int* misc;        // [8]: 0 = ntouched, 1 = abort flag
+    float* rinv;      // [2][8]: prescale inverses travelling with the partials
+    uint64_t* rfull;  // [2]: partials of a unit written (16 compute warps arrive)
+    uint64_t* rempty; // [2]: partial buffer read by the reducer
+    int* off_s;       // [257]: route offsets built in the kernel
+    int* perm_s;      // [512]: route list built in the kernel
 };
 
 __device__ inline Carve carve(unsigned char* base, const Plan& p, int K) {
     Carve c;
     unsigned char* q = base;
-    c.ring = q;                    q += static_cast<size_t>(p.nstages) * kStageBytes;
-    c.xs = q;                      q += static_cast<size_t>(p.tg) * p.xstride;
-    c.xsum = reinterpret_cast<float*>(q);    q += static_cast<size_t>(K / kBlockK) * 8 * 4;
-    c.xinv = reinterpret_cast<float*>(q);    q += 8 * 4;
-    c.red = reinterpret_cast<float*>(q);     q += 2 * kNCW * 2 * kRowTile * 8 * 4;
-    c.full = reinterpret_cast<uint64_t*>(q); q += kMaxStages * 8;
-    c.empty = reinterpret_cast<uint64_t*>(q); q += kMaxStages * 8;
-    c.touched = reinterpret_cast<int*>(q);   q += kMaxExperts * 4;
-    c.cnt = reinterpret_cast<int*>(q);       q += kMaxExperts * 4;
-    c.goff = reinterpret_cast<int*>(q);      q += (kMaxExperts + 1) * 4;
-    c.misc = reinterpret_cast<int*>(q);
+    // every region starts on a 16-byte boundary (the mbarriers need 8)
+    auto take = [&](size_t bytes) {
+        unsigned char* r = q;
+        q += (bytes + 15) & ~static_cast<size_t>(15);
+        return r;
+    };
+    c.ring = take(static_cast<size_t>(p.nstages) * kStageBytes);
+    c.xs = take(static_cast<size_t>(p.tg) * p.xstride);
+    c.xsum = reinterpret_cast<float*>(take(static_cast<size_t>(K / kBlockK) * 8 * 4));
+    c.xinv = reinterpret_cast<float*>(take(8 * 4));
+    c.red = reinterpret_cast<float*>(take(2 * kNCW * 2 * kRowTile * 8 * 4));
+    c.full = reinterpret_cast<uint64_t*>(take(kMaxStages * 8));
+    c.empty = reinterpret_cast<uint64_t*>(take(kMaxStages * 8));
+    c.rfull = reinterpret_cast<uint64_t*>(take(2 * 8));
+    c.rempty = reinterpret_cast<uint64_t*>(take(2 * 8));
+    c.touched = reinterpret_cast<int*>(take(kMaxExperts * 4));
+    c.cnt = reinterpret_cast<int*>(take(kMaxExperts * 4));
+    c.goff = reinterpret_cast<int*>(take((kMaxExperts + 1) * 4));
+    c.misc = reinterpret_cast<int*>(take(8 * 4));
+    c.rinv = reinterpret_cast<float*>(take(2 * 8 * 4));
+    c.off_s = reinterpret_cast<int*>(take((kMaxExperts + 1) * 4));
+    c.perm_s = reinterpret_cast<int*>(take(kMaxLocalRoutes * 4));
     return c;
 }
 
@@ -165,8 +185,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     Carve c = carve(smem_raw, p, K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- unit tables (touched experts, groups) ---------------------------------------------
+    // ---- route list (built here for decode sizes), unit tables --------------------------------
+    const int* OFF = a.off;
+    const int* PERM = a.perm;
+    if (a.idx) {
+        OFF = c.off_s;
+        PERM = c.perm_s;
+    }
     if (threadIdx.x == 0) {
+        if (a.idx) {
+            // counting sort of the route ids by expert, ascending id inside an expert
+            const int n = a.T * a.k;
+            for (int e = 0; e <= a.E; ++e) c.off_s[e] = 0;
+            for (int r = 0; r < n; ++r) {
+                const int e = a.idx[r];
+                if (e >= 0 && e < a.E) c.off_s[e + 1] += 1;
+                else report_error(a.status, DEV_ERR_INVALID);
+            }
+            for (int e = 0; e < a.E; ++e) c.off_s[e + 1] += c.off_s[e];
+            for (int e = 0; e < a.E; ++e) c.cnt[e] = c.off_s[e];     // cursors (cnt reused)
+            for (int r = 0; r < n; ++r) {
+                const int e = a.idx[r];
+                if (e >= 0 && e < a.E) c.perm_s[c.cnt[e]++] = r;
+            }
+        }
         int nt = 0, acc = 0;
         if (a.dense) {
             c.touched[0] = 0;
@@ -176,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             nt = 1;
         } else {
             for (int e = 0; e < a.E; ++e) {
-                const int n = a.off[e + 1] - a.off[e];
+                const int n = OFF[e + 1] - OFF[e];
                 if (n > 0) {
                     c.touched[nt] = e;
                     c.cnt[nt] = n;
@@ -193,14 +235,103 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             mbar_init(&c.full[s], 1);
             mbar_init(&c.empty[s], kNCW);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c.rfull[b], kNCW);
+            mbar_init(&c.rempty[b], 1);
+        }
         fence_mbar_init();
     }
+    // the phase-1 launch clears the combine counters the phase-2 launch will count with
+    if (a.cmb_mode == 1 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < a.cmb_n; i += blockDim.x) a.cmb_cnt[i] = 0;
     __syncthreads();
     const int nt = c.misc[0];
     const int U = RT * c.goff[nt];
     const int u0 = static_cast<int>((static_cast<long long>(U) * blockIdx.x) / gridDim.x);
     const int u1 = static_cast<int>((static_cast<long long>(U) * (blockIdx.x + 1)) / gridDim.x);
     if (u0 >= u1) return;
+
+    if (warp == kNCW + 1) {
+        // ================================ reducer warp ======================================
+        // Sums the 16 compute warps' partials of each unit in fixed warp order, applies the
+        // prescale inverse, bias and activation, stores the unit's outputs; in phase 2 of a
+        // routed decode call the last unit of each 16-row tile also runs the slot-ordered
+        // combine for that tile.
+        int j = 0;
+        for (int u = u0; u < u1; ++u) {
+            int rt, g;
+            decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
+            const int e = c.touched[j];
+            const int cnt_g = min(tg, c.cnt[j] - g * tg);
+            const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
+            const int nl = u - u0, b = nl & 1;
+            const bool ok = c.misc[1] == 0 && mbar_wait_bounded(&c.rfull[b], (nl >> 1) & 1);
+            if (!ok) {
+                if (lane == 0 && c.misc[1] == 0) {
+                    c.misc[1] = 1;
+                    report_error(a.status, DEV_ERR_TIMEOUT);
+                }
+            } else {
+                const float* redb = c.red + static_cast<size_t>(b) * kNCW * 2 * kRowTile * 8;
+                for (int o = lane; o < kRowTile * 8; o += 32) {
+                    const int n = o / kRowTile, row = o % kRowTile;
+                    if (n >= cnt_g) continue;
+                    const int rid = a.dense ? rbase + n : PERM[rbase + n];
+                    const int orow = rt * kRowTile + row;
+                    float s0 = 0.0f, s1 = 0.0f;
+                    for (int w = 0; w < kNCW; ++w) {
+                        s0 += redb[(w * 2 + 0) * kRowTile * 8 + row * 8 + n];
+                        if (nmat == 2) s1 += redb[(w * 2 + 1) * kRowTile * 8 + row * 8 + n];
+                    }
+                    const float inv = c.rinv[b * 8 + n];
+                    s0 *= inv;
+                    s1 *= inv;
+                    const size_t bidx = static_cast<size_t>(e) * R + orow;
+                    if (a.b0) s0 += __bfloat162float(__ushort_as_bfloat16(a.b0[bidx]));
+                    if (a.phase == 0) {
+                        if (a.b1) s1 += __bfloat162float(__ushort_as_bfloat16(a.b1[bidx]));
+                        const float h = act_fn(a.act, s0, s1, a.limit, a.alpha);
+                        static_cast<uint16_t*>(a.out)[static_cast<size_t>(rid) * R + orow] = float_to_adt_bits(h, a.adt);
+                    } else {
+                        static_cast<float*>(a.out)[static_cast<size_t>(rid) * R + orow] = s0;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.rempty[b]);
+        }
+        if (a.cmb_mode == 2 && c.misc[1] == 0) {
+            // Fused combine: every unit of a 16-row tile (over all CTAs) bumps that tile's
+            // counter once this CTA's outputs are globally visible (one fence for all of them);
+            // the CTA that completes a tile's count runs the slot-ordered combine for it.
+            __threadfence();
+            __syncwarp();
+            j = 0;
+            for (int u = u0; u < u1; ++u) {
+                int rt, g;
+                decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
+                int last = 0;
+                if (lane == 0) last = (atomicAdd(a.cmb_cnt + rt, 1) + 1 == c.goff[nt]);
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (!last) continue;
+                __threadfence();
+                const float* ev = static_cast<const float*>(a.out);
+                for (int o = lane; o < a.T * kRowTile; o += 32) {
+                    const int t = o / kRowTile, orow = rt * kRowTile + o % kRowTile;
+                    const size_t yo = static_cast<size_t>(t) * R + orow;
+                    float accv = a.seed ? __ldcg(a.seed + yo) : 0.0f;
+                    for (int q = 0; q < a.k; ++q) {
+                        const size_t r = static_cast<size_t>(t) * a.k + q;
+                        accv = __fadd_rn(accv, __fmul_rn(a.w[r], __ldcg(ev + r * R + orow)));
+                    }
+                    if (a.y_f32) a.y_f32[yo] = accv;
+                    static_cast<uint16_t*>(a.y)[yo] = float_to_adt_bits(accv, a.adt);
+                }
+                if (lane == 0) a.cmb_cnt[rt] = 0;
+            }
+        }
+        return;
+    }
 
     if (warp == kNCW) {
         // ================================ producer warp =====================================
@@ -267,17 +398,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
         const int e = c.touched[j];
         const int cnt_g = min(tg, c.cnt[j] - g * tg);
-        const int rbase = a.dense ? g * tg : a.off[e] + g * tg;
+        const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
 
         // ---- stage this group's activations (f16 with prescale, or as-is) -----------------
         if (j != staged_j || g != staged_g) {
+            // every compute warp must be done with the previous group's activations
+            if (staged_j >= 0) named_bar(1, kNCW * 32);
             staged_j = j;
             staged_g = g;
             if (warp < 8) {
                 const int n = warp;
                 float inv = 0.0f;
                 if (n < cnt_g) {
-                    const int rid = a.dense ? rbase + n : a.perm[rbase + n];
+                    const int rid = a.dense ? rbase + n : PERM[rbase + n];
                     size_t row;
                     if (a.phase == 0) row = a.dense ? static_cast<size_t>(rid) : static_cast<size_t>(rid / a.k);
                     else row = static_cast<size_t>(rid);
@@ -450,12 +583,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             }
         }
 
-        // ---- cross-warp reduction (fixed order) + epilogue ------------------------------------
-        // two reduction buffers alternate between units: the barrier of unit u+1 proves every
-        // reader of unit u's buffer is done before unit u+2 overwrites it
-        float* redb = c.red + static_cast<size_t>(u & 1) * kNCW * 2 * kRowTile * 8;
+        // ---- hand the partials to the reducer warp (double-buffered, no CTA barrier) ---------
         {
-            float* rw = redb + static_cast<size_t>(warp) * 2 * kRowTile * 8;
+            const int nl = u - u0, b = nl & 1;
+            const bool ok = c.misc[1] == 0 && mbar_wait_bounded(&c.rempty[b], ((nl >> 1) & 1) ^ 1);
+            if (!ok) {
+                if (lane == 0 && c.misc[1] == 0) {
+                    c.misc[1] = 1;
+                    report_error(a.status, DEV_ERR_TIMEOUT);
+                }
+            }
+            float* rw = c.red + (static_cast<size_t>(b) * kNCW + warp) * 2 * kRowTile * 8;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 if (m >= nmat) break;
@@ -465,31 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 rm[(gid + 8) * 8 + 2 * tid] = acc[m][2];
                 rm[(gid + 8) * 8 + 2 * tid + 1] = acc[m][3];
             }
-        }
-        named_bar(1, kNCW * 32);
-        if (threadIdx.x < kRowTile * 8 && c.misc[1] == 0) {
-            const int n = threadIdx.x / kRowTile, row = threadIdx.x % kRowTile;
-            if (n < cnt_g) {
-                const int rid = a.dense ? rbase + n : a.perm[rbase + n];
-                const int orow = rt * kRowTile + row;
-                float s0 = 0.0f, s1 = 0.0f;
-                for (int w = 0; w < kNCW; ++w) {
-                    s0 += redb[(w * 2 + 0) * kRowTile * 8 + row * 8 + n];
-                    if (nmat == 2) s1 += redb[(w * 2 + 1) * kRowTile * 8 + row * 8 + n];
-                }
-                const float inv = c.xinv[n];
-                s0 *= inv;
-                s1 *= inv;
-                const size_t bidx = static_cast<size_t>(e) * R + orow;
-                if (a.b0) s0 += __bfloat162float(__ushort_as_bfloat16(a.b0[bidx]));
-                if (a.phase == 0) {
-                    if (a.b1) s1 += __bfloat162float(__ushort_as_bfloat16(a.b1[bidx]));
-                    const float h = act_fn(a.act, s0, s1, a.limit, a.alpha);
-                    static_cast<uint16_t*>(a.out)[static_cast<size_t>(rid) * R + orow] = float_to_adt_bits(h, a.adt);
-                } else {
-                    static_cast<float*>(a.out)[static_cast<size_t>(rid) * R + orow] = s0;
-                }
-            }
+            if (warp == 0 && lane < 8) c.rinv[b * 8 + lane] = c.xinv[lane];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.rfull[b]);
         }
     }
 }

@@ -67,6 +67,15 @@ struct GemvArgs {
     int dense;                    // 1: every token routed to expert 0 (shared expert)
     int tg;                       // tokens per unit group (1..8)
     int* status;
+    const int32_t* idx;           // [T][k]: build the route list in the kernel (T*k <= 512), or
+                                  // nullptr: use off/perm
+    int cmb_mode;                 // 0 none; 1 (phase 1) clear cmb_cnt; 2 (phase 2) fused combine
+    int* cmb_cnt;                 // per-row-tile unit counters of phase 2 (H / 16 of them)
+    int cmb_n;                    // number of counters (H / 16)
+    const float* w;               // combine: routing weights [T][k]
+    const float* seed;            // combine: shared-expert output [T][H] or nullptr
+    void* y;                      // combine: [T][H] adt
+    float* y_f32;                 // combine: [T][H] or nullptr
 };
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s);
 size_t gemv_smem_bytes(int fmt, int K, int tg);

@@ -119,15 +119,52 @@ def ulp16(v, adt):
     return np.ldexp(1.0, (e - (p - 1)).astype(np.int64))
 
 
-def check_outputs(y_gpu_f64, y32_gpu_f64, y_ref_bits_f64, y32_ref_f64, adt, max_abs=2e-2, rel_l2=1e-3):
+def check_outputs(y_gpu_f64, y32_gpu_f64, y_ref_bits_f64, y32_ref_f64, adt, max_abs=2e-2, rel_l2=1e-3,
+                  flip_bound=None):
     """The parity bar: f32 outputs within max-abs and rel-L2; 16-bit outputs within the same
     bars, except that an element may differ by one unit in the last place of the 16-bit type
-    (both sides round an f32 sum; sums a hair apart can straddle a rounding boundary)."""
-    mx, rel = parity_metrics(y32_gpu_f64, y32_ref_f64)
-    assert mx <= max_abs and rel <= rel_l2, ("f32 outputs", mx, rel)
-    d = np.abs(y_gpu_f64 - y_ref_bits_f64)
-    allow = np.maximum(max_abs, ulp16(y_ref_bits_f64, adt))
-    assert np.all(d <= allow), ("16-bit outputs", float(d.max()))
+    (both sides round an f32 sum; sums a hair apart can straddle a rounding boundary).
+
+    flip_bound: both sides also round the intermediate h to 16 bits; where an h element sits
+    next to a rounding boundary the two sides can round it to neighbouring values, which moves
+    the outputs that depend on it by up to ulp16(h) * |W_d| -- one such flip shifts a whole
+    output row of that token.  With flip_bound set, elements beyond max_abs are accepted if they
+    are at most 2 % of the outputs and each stays within flip_bound; rel-L2 is never relaxed."""
+    def within(a, b, extra):
+        d = np.abs(a - b)
+        allow = np.maximum(max_abs, extra)
+        bad = d > allow
+        if flip_bound is not None and bad.any():
+            ok = bad.sum() <= max(1, int(0.02 * d.size)) and np.all(d[bad] <= flip_bound)
+            return ok, float(d.max()), int(bad.sum())
+        return not bad.any(), float(d.max()), int(bad.sum())
+    ok, dmax, nbad = within(y32_gpu_f64, y32_ref_f64, 0.0)
+    rel = np.linalg.norm(y32_gpu_f64 - y32_ref_f64) / max(np.linalg.norm(y32_ref_f64), 1e-30)
+    assert ok and rel <= rel_l2, ("f32 outputs", dmax, nbad, rel)
+    ok, dmax16, nbad16 = within(y_gpu_f64, y_ref_bits_f64, ulp16(y_ref_bits_f64, adt))
+    assert ok, ("16-bit outputs", dmax16, nbad16)
     rel16 = np.linalg.norm(y_gpu_f64 - y_ref_bits_f64) / max(np.linalg.norm(y_ref_bits_f64), 1e-30)
     assert rel16 <= rel_l2, ("16-bit rel-L2", rel16)
-    return mx, rel
+    return dmax, rel
+
+
+def h_flip_bound(oex, xin_f64_rows, idx_rows, adt, down_f64_absmax):
+    """2 * ulp16(max |h|) * max |W_d|: the most two neighbouring-value roundings of h can move
+    one output (routing weights are at most 1).  max |h| from the oracle's own h of the routes."""
+    import oracle
+    hmax = 0.0
+    for xrow, sel in zip(xin_f64_rows, idx_rows):
+        for e in sel:
+            h, _ = oracle.expert_ffn(oex, int(e), xrow, adt)
+            hmax = max(hmax, float(np.abs(h).max()))
+    return 2.0 * float(ulp16(hmax, adt)) * down_f64_absmax
+
+
+def weight_absmax(fmt, codes, scales=None):
+    """An upper bound of |W| over a canonical weight tensor, computed without dequantising it."""
+    if fmt in ("f16", "bf16"):
+        return float(codes.abs().max().item())
+    if fmt == "mxfp4":
+        return 6.0 * 2.0 ** (int(scales.max().item()) - 127)
+    sm = scales.float()
+    return float(torch.maximum(sm[..., 1].abs(), (15.0 * sm[..., 0] + sm[..., 1]).abs()).max().item())

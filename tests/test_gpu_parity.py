@@ -13,8 +13,8 @@ import torch
 
 import oracle
 from mixture_experts_routed_logits_gb300 import synth
-from tests._helpers import (bits16, check_outputs, gpu_layer, oracle_layer, oracle_route,
-                            parity_metrics, to_device)
+from tests._helpers import (bits16, check_outputs, gpu_layer, h_flip_bound, oracle_layer,
+                            oracle_route, parity_metrics, to_device, weight_absmax)
 
 pytestmark = pytest.mark.gpu
 
@@ -129,8 +129,15 @@ def test_forward_parity(case):
     rows = slice(None) if toks is None else toks
     g32 = y32.double().cpu().numpy()[rows]
     gy = oracle.adt_bits_to_f64(bits16(y)[rows], c["adt"])
+    fb = None
+    if toks is not None:
+        # large case: bound the effect of h rounding flips from the oracle's own h
+        ex_d = L["experts"]
+        wd_max = weight_absmax(c["fmt"], ex_d["down"], ex_d.get("down_s"))
+        fb = h_flip_bound(oex, oracle.adt_bits_to_f64(xin[toks][:2], c["adt"]), oidx[toks][:2],
+                          c["adt"], wd_max)
     check_outputs(gy, g32, oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"],
-                  MAX_ABS, REL_L2)
+                  MAX_ABS, REL_L2, flip_bound=fb)
     assert moe.device_status(ws) == 0
 
 
