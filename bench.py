@@ -40,6 +40,8 @@ def parse():
     p.add_argument("--T", type=int, default=None)
     p.add_argument("--layers", type=int, default=None, help="rotating weight sets")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"],
+                   help="expert path passed to ts_moe_forward_path")
     p.add_argument("--profile", action="store_true",
                    help="short run for profiler captures: one timed repetition, few samples")
     return p.parse_args()
@@ -259,7 +261,7 @@ def main():
                          out=(ly["idx"], ly["w"], ly["xn"], None), stream=stream)
         xin = ly["xn"] if cfg["rmsnorm"] else L["x"]
         moe.forward(xin, ly["ex"], ly["idx"], ly["w"], shared=ly["sh"], ws=ly["ws"],
-                    out=(ly["y"], None), stream=stream)
+                    out=(ly["y"], None), path=args.path, stream=stream)
 
     # ---- CUDA graphs: one per layer, plus a copy with per-phase events -------------------------------
     nph = 7
@@ -288,12 +290,14 @@ def main():
     flush = synth.make_l2_flush("cuda")
     # the library's automatic choice: tensor-core grouped GEMM above 8 tokens for MXFP4 and for
     # 16-bit weights of the activation type (H, I multiples of 64), else the streaming GEMV
-    gemm_path = (T > 8 and H % 64 == 0 and I % 64 == 0
-                 and (cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"]))
+    gemm_ok = H % 64 == 0 and I % 64 == 0 and (cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"])
+    gemm_path = gemm_ok and (args.path == "gemm" or (args.path == "auto" and T > 8))
     # GEMV decode (T*k <= 512): router, phase 1, phase 2 (+ fused route list and combine);
     # otherwise router, route list, [gather], phase 1, phase 2, combine; + 2 shared-expert GEMVs
     fused_decode = (not gemm_path) and T * k <= 512
-    n_launch_step = (3 if fused_decode else 5 + (1 if gemm_path else 0)) + (2 if cfg.get("shared_I") else 0)
+    n_launch_step = ((3 if fused_decode else 5 + (1 if gemm_path else 0)
+                      + (1 if gemm_path and cfg["fmt"] == "mxfp4" else 0))
+                     + (2 if cfg.get("shared_I") else 0))
 
     def timed(K):
         b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]

@@ -89,8 +89,12 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
 }
 
 struct WsLayout {
-    size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hmax, hinv, h16, cmb, total;
+    size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hmax, hinv, h16, cmb, part, tcnt, total;
+    size_t tcnt_n;        // split-K group counters per phase
+    int max_split;        // > 1 when the partials fit (decode sizes)
 };
+
+constexpr int kMaxSplit = 8;
 
 WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts* sh) {
     WsLayout L{};
@@ -354,7 +358,11 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         G.status = status;
         G.col_scale = xinv;
         G.hmax = hmax;
-        e = launch_tc_gemm(G, sms, st);
+        G.max_split = L.max_split;
+        G.part = L.max_split > 1 ? reinterpret_cast<float*>(W + L.part) : nullptr;
+        G.cnt = L.max_split > 1 ? reinterpret_cast<int*>(W + L.tcnt) : nullptr;
+        if (L.max_split > 1) e = cudaMemsetAsync(W + L.tcnt, 0, 2 * L.tcnt_n * 4, st);
+        if (e == cudaSuccess) e = launch_tc_gemm(G, sms, st);
         if (e == cudaSuccess) e = phase_mark(1, st);
         if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: tensor-core phase 1");
         G.phase = 1;
@@ -368,6 +376,7 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         G.act_in = W + L.h;
         G.out = W + L.e;
         G.hmax = nullptr;
+        if (L.max_split > 1) G.cnt = reinterpret_cast<int*>(W + L.tcnt) + L.tcnt_n;
         if (quant_gemm) {
             uint16_t* h16 = reinterpret_cast<uint16_t*>(W + L.h16);
             float* hinv = reinterpret_cast<float*>(W + L.hinv);

@@ -43,24 +43,29 @@ namespace {
 constexpr int kBM = 128;                         // weight rows per accumulator
 constexpr int kBN = 256;                         // max routes per tile
 constexpr int kBK = 64;                          // K elements per stage (128 bytes of 16-bit)
-constexpr int kStages = 3;
 constexpr int kATile = kBM * kBK * 2;            // 16 KB
 constexpr int kBBox = 64 * kBK * 2;              // 8 KB: one 64-row TMA box of activations
-constexpr int kStage = 2 * kATile + (kBN / 64) * kBBox;   // 64 KB
 constexpr int kThreads = 192;
-// QUANT variant: + staging of the packed tiles (2 tiles x 8 row tiles x 2 blocks x 272 B),
-// stage rounded to 1 KB so every A tile stays 1024-byte aligned for the 128B swizzle
+// QUANT variant: a packed slot holds the B boxes and two 8-row-tile x 2-block packed tiles
 constexpr int kPackBlk = 272;
 constexpr int kStaging = 2 * 8 * 2 * kPackBlk;             // 8704 B
-constexpr int kStageQ = (kStage + kStaging + 1023) / 1024 * 1024;
-constexpr int kThreadsQ = 320;                              // + 4 dequant warps
-constexpr int kDqWarps = 4;
+constexpr int kThreadsQ = 448;                              // + 8 dequant warps
+constexpr int kDqWarps = 8;
+
+struct TcLayout {        // host-chosen shape of one launch
+    int bn;              // routes per tile (64 or 256)
+    int nslot;           // stages (16-bit weights) or packed slots (MXFP4)
+    int slot_bytes;      // bytes per stage / slot (multiple of 1024)
+    int a_ring_bytes;    // MXFP4: two dequantised A stages (64 KB); else 0
+    int S;               // K split into S parts (partials reduced by the group's last CTA)
+};
 
 struct TcParams {
     CUtensorMap tmA0;     // phase 1: gate [E][I][H]; phase 2: down [E][H][I]
     CUtensorMap tmA1;     // phase 1: up; phase 2: unused (down again)
     CUtensorMap tmB;      // sorted activations [Tk][K]
     GemmArgs a;
+    TcLayout ly;
 };
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
@@ -122,18 +127,27 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-    uint32_t r[16];
+// Two 16-column loads (rows of this warp's lane quarter), one wait for both.
+__device__ __forceinline__ void tmem_ld16_pair(uint32_t ta, uint32_t tb, float va[16], float vb[16]) {
+    uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15}, [%16];"
+        "%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+        "%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[16 + i]);
+    }
 }
 
 __device__ __forceinline__ float act_fn(int act, float g, float u, float limit, float alpha) {
@@ -147,10 +161,13 @@ __device__ __forceinline__ float act_fn(int act, float g, float u, float limit, 
     return g / (1.0f + expf(-alpha * g)) * (u + 1.0f);
 }
 
+constexpr int kMaxSlots = 8;
+
 struct SmemTail {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t dq[kStages];           // QUANT: A tiles dequantised
+    uint64_t full[kMaxSlots];       // stage / packed slot loaded
+    uint64_t empty[kMaxSlots];      // stage / packed slot consumed by the MMA
+    uint64_t afull[2];              // QUANT: dequantised A stage written
+    uint64_t aempty[2];             // QUANT: dequantised A stage consumed by the MMA
     uint64_t tfull;
     uint64_t tempty;
     uint32_t tmem_base;
@@ -158,6 +175,7 @@ struct SmemTail {
     int nt;                         // touched experts
     int touched[kMaxExperts];
     int cnt[kMaxExperts];
+    int bnj[kMaxExperts];           // routes per tile of each touched expert (<= bn)
     int ioff[kMaxExperts + 1];      // item prefix per touched expert
 };
 
@@ -165,36 +183,47 @@ template <bool QUANT>
 __global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    constexpr int SB = QUANT ? kStageQ : kStage;            // bytes per stage
+    const TcLayout& Ly = P.ly;
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SmemTail* tl = reinterpret_cast<SmemTail*>(base + kStages * SB);
+    unsigned char* ring = base + Ly.a_ring_bytes;           // stages (16-bit) / packed slots
+    SmemTail* tl = reinterpret_cast<SmemTail*>(ring + static_cast<size_t>(Ly.nslot) * Ly.slot_bytes);
     const GemmArgs& a = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = a.R, K = a.K;
     const int rows_per_item = a.phase == 0 ? kBM : 2 * kBM;
     const int MB = (R + rows_per_item - 1) / rows_per_item;
     const int nkb = K / kBK;
+    const int NS = Ly.nslot, BN = Ly.bn, S = Ly.S;
+    const int kbp = (nkb + S - 1) / S;                      // stages per K part
+    const int bbytes = (BN / 64) * kBBox;                   // B area of a stage / slot
 
     if (threadIdx.x == 0) {
         int nt = 0, acc = 0;
         for (int e = 0; e < a.E; ++e) {
             const int n = a.off[e + 1] - a.off[e];
             if (n > 0) {
+                // the expert's routes in equal tiles (multiples of 16), not full tiles + a tail
+                const int ntl0 = (n + BN - 1) / BN;
+                const int bnj = min(BN, ((n + ntl0 - 1) / ntl0 + 15) & ~15);
                 tl->touched[nt] = e;
                 tl->cnt[nt] = n;
+                tl->bnj[nt] = bnj;
                 tl->ioff[nt] = acc;
-                acc += MB * ((n + kBN - 1) / kBN);
+                acc += MB * ((n + bnj - 1) / bnj) * S;
                 ++nt;
             }
         }
         tl->ioff[nt] = acc;
         tl->nt = nt;
         tl->abort_flag = 0;
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&tl->full[s], 1);
             mbar_init(&tl->empty[s], 1);
-            mbar_init(&tl->dq[s], kDqWarps);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&tl->afull[s], kDqWarps);
+            mbar_init(&tl->aempty[s], 1);
         }
         mbar_init(&tl->tfull, 1);
         mbar_init(&tl->tempty, 4);
@@ -214,13 +243,17 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     const int nt = tl->nt;
     const int items = tl->ioff[nt];
 
-    auto decode = [&](int i, int& j, int& mb, int& tile) {
+    // item i -> touched expert j, row block mb, route tile, K part kp (kp fastest: the S parts
+    // of one output tile are consecutive items, group = i / S)
+    auto decode = [&](int i, int& j, int& mb, int& tile, int& kp) {
         j = 0;
         while (j + 1 < nt && i >= tl->ioff[j + 1]) ++j;
-        const int ntl = (tl->cnt[j] + kBN - 1) / kBN;
+        const int ntl = (tl->cnt[j] + tl->bnj[j] - 1) / tl->bnj[j];
         const int local = i - tl->ioff[j];
-        mb = local / ntl;
-        tile = local % ntl;
+        kp = local % S;
+        const int rest = local / S;
+        tile = rest % ntl;
+        mb = rest / ntl;
     };
 
     if (warp == 0) {
@@ -228,59 +261,59 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             // =============================== TMA producer ====================================
             int it = 0;
             for (int i = blockIdx.x; i < items && !tl->abort_flag; i += gridDim.x) {
-                int j, mb, tile;
-                decode(i, j, mb, tile);
+                int j, mb, tile, kp;
+                decode(i, j, mb, tile, kp);
                 const int e = tl->touched[j];
-                const int p0 = a.off[e] + tile * kBN;
-                const int n_valid = min(kBN, tl->cnt[j] - tile * kBN);
+                const int p0 = a.off[e] + tile * tl->bnj[j];
+                const int n_valid = min(tl->bnj[j], tl->cnt[j] - tile * tl->bnj[j]);
                 const int nbox = (n_valid + 63) / 64;
                 const int r0 = mb * rows_per_item;
                 const int r1 = a.phase == 0 ? r0 : r0 + kBM;
-                const int RT = R / kRowTile;                // 16-row tiles per expert matrix
-                const int nblk = K / kBlockK;
-                (void)RT;
-                (void)nblk;
+                const int kb0 = kp * kbp, kb1 = min(nkb, kb0 + kbp);
                 const uint32_t bytes = (QUANT ? 2 * 8 * 2 * kPackBlk : 2 * kATile) + nbox * kBBox;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % kStages;
-                    if (!mbar_wait_bounded(&tl->empty[s], ((it / kStages) & 1) ^ 1)) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % NS;
+                    if (!mbar_wait_bounded(&tl->empty[s], ((it / NS) & 1) ^ 1)) {
                         tl->abort_flag = 1;
                         report_error(a.status, DEV_ERR_TIMEOUT);
                         break;
                     }
-                    unsigned char* st = base + s * SB;
+                    unsigned char* st = ring + static_cast<size_t>(s) * Ly.slot_bytes;
                     mbar_arrive_expect_tx(&tl->full[s], bytes);
+                    unsigned char* bdst;
                     if (QUANT) {
-                        // one TMA per matrix: 8 packed 16-row tiles x 2 blocks (4352 bytes); row
-                        // tiles past the matrix come back zero-filled
-                        unsigned char* stg = st + kStage;
+                        // slot = [B boxes | packed A0 (8 row tiles x 2 blocks) | packed A1];
+                        // row tiles past the matrix come back zero-filled
+                        unsigned char* stg = st + bbytes;
                         tma_load_3d(stg, &P.tmA0, 2 * kb * (kPackBlk / 4), r0 / kRowTile, e, &tl->full[s]);
                         tma_load_3d(stg + 8 * 2 * kPackBlk, a.phase == 0 ? &P.tmA1 : &P.tmA0,
                                     2 * kb * (kPackBlk / 4), r1 / kRowTile, e, &tl->full[s]);
+                        bdst = st;
                     } else {
                         tma_load_3d(st, &P.tmA0, kb * kBK, r0, e, &tl->full[s]);
                         tma_load_3d(st + kATile, a.phase == 0 ? &P.tmA1 : &P.tmA0, kb * kBK, r1, e,
                                     &tl->full[s]);
+                        bdst = st + 2 * kATile;
                     }
                     for (int q = 0; q < nbox; ++q)
-                        tma_load_2d(st + 2 * kATile + q * kBBox, &P.tmB, kb * kBK, p0 + 64 * q,
-                                    &tl->full[s]);
+                        tma_load_2d(bdst + q * kBBox, &P.tmB, kb * kBK, p0 + 64 * q, &tl->full[s]);
                 }
             }
-            // drain: the last stages' copies must land before the CTA may exit
-            for (int q = (it > kStages ? it - kStages : 0); q < it; ++q)
-                mbar_wait_bounded(&tl->full[q % kStages], (q / kStages) & 1);
+            // drain: the last slots' copies must land before the CTA may exit
+            for (int q = (it > NS ? it - NS : 0); q < it; ++q)
+                mbar_wait_bounded(&tl->full[q % NS], (q / NS) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ================================= MMA issuer ====================================
             int it = 0, n_item = 0;
             for (int i = blockIdx.x; i < items && !tl->abort_flag; i += gridDim.x, ++n_item) {
-                int j, mb, tile;
-                decode(i, j, mb, tile);
-                const int n_valid = min(kBN, tl->cnt[j] - tile * kBN);
+                int j, mb, tile, kp;
+                decode(i, j, mb, tile, kp);
+                const int n_valid = min(tl->bnj[j], tl->cnt[j] - tile * tl->bnj[j]);
                 const int N = (n_valid + 15) & ~15;
                 const uint32_t idesc = idesc_f16kind(a.ab_bf16, kBM, N);
+                const int kb0 = kp * kbp, kb1 = min(nkb, kb0 + kbp);
                 if (!mbar_wait_bounded(&tl->tempty, (n_item & 1) ^ 1)) {
                     tl->abort_flag = 1;
                     report_error(a.status, DEV_ERR_TIMEOUT);
@@ -288,91 +321,106 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 }
                 tc_fence_after();
                 bool ok = true;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % kStages;
-                    if (!mbar_wait_bounded(QUANT ? &tl->dq[s] : &tl->full[s], (it / kStages) & 1)) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % NS, sa = it & 1;
+                    const bool got = QUANT ? mbar_wait_bounded(&tl->afull[sa], (it >> 1) & 1)
+                                           : mbar_wait_bounded(&tl->full[s], (it / NS) & 1);
+                    if (!got) {
                         tl->abort_flag = 1;
                         report_error(a.status, DEV_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(base + s * SB);
-                    const uint64_t d0 = sdesc_sw128(sa);
-                    const uint64_t d1 = sdesc_sw128(sa + kATile);
-                    const uint64_t db = sdesc_sw128(sa + 2 * kATile);
+                    const unsigned char* st = ring + static_cast<size_t>(s) * Ly.slot_bytes;
+                    const uint32_t sa0 = smem_u32(QUANT ? base + sa * 2 * kATile : st);
+                    const uint64_t d0 = sdesc_sw128(sa0);
+                    const uint64_t d1 = sdesc_sw128(sa0 + kATile);
+                    const uint64_t db = sdesc_sw128(smem_u32(QUANT ? st : st + 2 * kATile));
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks) {
-                        const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+                        const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
                         umma(tmem, d0 + 2 * ks, db + 2 * ks, idesc, acc);
                         umma(tmem + 256, d1 + 2 * ks, db + 2 * ks, idesc, acc);
                     }
-                    umma_commit(&tl->empty[s]);     // frees the stage once these MMAs are done
+                    umma_commit(&tl->empty[s]);         // frees the slot once these MMAs are done
+                    if (QUANT) umma_commit(&tl->aempty[sa]);
                 }
                 if (!ok) break;
-                umma_commit(&tl->tfull);            // accumulators ready for the epilogue
+                umma_commit(&tl->tfull);                // accumulators ready for the epilogue
             }
         }
     } else if (QUANT && warp >= 6) {
         // ======================= dequant warps (QUANT): packed e2m1 -> f16 A tiles =============
         const int dw = warp - 6;
         const int gid = lane >> 2, tid = lane & 3;
+        const int bb = dw & 1;
+        // rows gid (+8) of a row tile: (row & 7) == gid, so the swizzled chunk is fixed per lane
+        const int sw_off = gid * 128 + (((4 * bb + tid) ^ gid) << 4);
         int it = 0;
         bool bad_scale = false;
         const int RTm = R / kRowTile;               // 16-row tiles that exist per matrix
         for (int i = blockIdx.x; i < items && !tl->abort_flag; i += gridDim.x) {
-            int j, mb, tile_i;
-            decode(i, j, mb, tile_i);
+            int j, mb, tile_i, kp;
+            decode(i, j, mb, tile_i, kp);
             const int rt0 = (mb * rows_per_item) / kRowTile;
             const int rt1 = a.phase == 0 ? rt0 : rt0 + kBM / kRowTile;
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int s = it % kStages;
-                if (!mbar_wait_bounded(&tl->full[s], (it / kStages) & 1)) {
+            const int kb0 = kp * kbp, kb1 = min(nkb, kb0 + kbp);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % NS, sa = it & 1;
+                if (!mbar_wait_bounded(&tl->full[s], (it / NS) & 1) ||
+                    !mbar_wait_bounded(&tl->aempty[sa], ((it >> 1) & 1) ^ 1)) {
                     if (lane == 0) {
                         tl->abort_flag = 1;
                         report_error(a.status, DEV_ERR_TIMEOUT);
                     }
                     break;
                 }
-                unsigned char* st = base + s * SB;
-                const unsigned char* stg = st + kStage;
-#pragma unroll 2
-                for (int qb = dw; qb < 32; qb += kDqWarps) {
-                    const int tile = qb >> 4, rt = (qb >> 1) & 7, bb = qb & 1;
-                    // row tiles past the matrix were not copied: their A rows only feed output
-                    // rows that are never stored, so they are left as they are
+                const unsigned char* stg = ring + static_cast<size_t>(s) * Ly.slot_bytes + bbytes;
+                unsigned char* adst = base + sa * 2 * kATile;
+                // this warp: block column bb = dw & 1 of row tiles (dw >> 1) and (dw >> 1) + 4 of
+                // both tiles; the 128B swizzle puts 16-byte chunk c of row r at c ^ (r & 7)
+#pragma unroll
+                for (int qi = 0; qi < 4; ++qi) {
+                    const int tile = qi >> 1;
+                    const int rt = (dw >> 1) + 4 * (qi & 1);
+                    // row tiles past the matrix only feed output rows that are never stored
                     if ((tile == 0 ? rt0 : rt1) + rt >= RTm) continue;
                     const unsigned char* blk = stg + (tile * 8 + rt) * 2 * kPackBlk + bb * kPackBlk;
                     const uint2 cw = *reinterpret_cast<const uint2*>(blk + lane * 8);
                     const uint32_t sc = *reinterpret_cast<const uint16_t*>(blk + 256 + gid * 2);
                     const uint32_t e0 = sc & 0xFF, e1 = sc >> 8;
-                    // scaled e2m1 values are exact f16 numbers only for scales 2^-23 .. 2^13
-                    bad_scale |= (e0 < 104u) | (e0 > 140u) | (e1 < 104u) | (e1 > 140u);
-                    const __half2 s0 = __half2half2(__float2half_rn(e8m0_to_float(e0)));
-                    const __half2 s1 = __half2half2(__float2half_rn(e8m0_to_float(e1)));
-                    uint32_t va[4], vb[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t ra = e2m1x2_to_f16x2(cw.x >> (8 * j));
-                        uint32_t rb = e2m1x2_to_f16x2(cw.y >> (8 * j));
-                        __half2 ha = __hmul2(*reinterpret_cast<__half2*>(&ra), s0);
-                        __half2 hb = __hmul2(*reinterpret_cast<__half2*>(&rb), s1);
-                        va[j] = *reinterpret_cast<uint32_t*>(&ha);
-                        vb[j] = *reinterpret_cast<uint32_t*>(&hb);
+                    uint32_t s0, s1;            // f16x2 scales
+                    if (__all_sync(0xffffffffu, e0 >= 113u && e0 <= 140u && e1 >= 113u && e1 <= 140u)) {
+                        // normal f16 powers of two: exponent field e - 112, both halves at once
+                        s0 = (e0 - 112u) * 0x04000400u;
+                        s1 = (e1 - 112u) * 0x04000400u;
+                    } else {
+                        // scaled e2m1 values are exact f16 numbers only for scales 2^-23 .. 2^13
+                        bad_scale |= (e0 < 104u) | (e0 > 140u) | (e1 < 104u) | (e1 > 140u);
+                        const __half2 h0 = __half2half2(__float2half_rn(e8m0_to_float(e0)));
+                        const __half2 h1 = __half2half2(__float2half_rn(e8m0_to_float(e1)));
+                        s0 = *reinterpret_cast<const uint32_t*>(&h0);
+                        s1 = *reinterpret_cast<const uint32_t*>(&h1);
                     }
-                    // 128B swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
-                    unsigned char* at = st + tile * kATile;
-                    const int ra_row = rt * kRowTile + gid, rb_row = ra_row + 8;
-                    const int c = 4 * bb + tid;
-                    *reinterpret_cast<uint4*>(at + ra_row * 128 + ((c ^ (ra_row & 7)) << 4)) =
-                        make_uint4(va[0], va[1], va[2], va[3]);
-                    *reinterpret_cast<uint4*>(at + rb_row * 128 + ((c ^ (rb_row & 7)) << 4)) =
-                        make_uint4(vb[0], vb[1], vb[2], vb[3]);
+                    uint32_t ra[4], rb[4], va[4], vb[4];
+                    e2m1x8_to_f16x2x4(cw.x, ra);
+                    e2m1x8_to_f16x2x4(cw.y, rb);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        __half2 ha = __hmul2(*reinterpret_cast<__half2*>(&ra[q]), *reinterpret_cast<const __half2*>(&s0));
+                        __half2 hb = __hmul2(*reinterpret_cast<__half2*>(&rb[q]), *reinterpret_cast<const __half2*>(&s1));
+                        va[q] = *reinterpret_cast<uint32_t*>(&ha);
+                        vb[q] = *reinterpret_cast<uint32_t*>(&hb);
+                    }
+                    unsigned char* at = adst + tile * kATile + rt * (kRowTile * 128) + sw_off;
+                    *reinterpret_cast<uint4*>(at) = make_uint4(va[0], va[1], va[2], va[3]);
+                    *reinterpret_cast<uint4*>(at + 8 * 128) = make_uint4(vb[0], vb[1], vb[2], vb[3]);
                 }
                 // generic-proxy stores must be visible to the tensor core's async-proxy reads
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tl->dq[s]);
+                if (lane == 0) mbar_arrive(&tl->afull[sa]);
             }
         }
         if (__any_sync(0xffffffffu, bad_scale) && lane == 0) report_error(a.status, DEV_ERR_UNSUPPORTED);
@@ -380,13 +428,14 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         // =================================== epilogue ==========================================
         const int q = warp & 3;                     // TMEM lane quarter this warp may access
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const int Tk = a.rows_in;
         int n_item = 0;
         for (int i = blockIdx.x; i < items; i += gridDim.x, ++n_item) {
-            int j, mb, tile;
-            decode(i, j, mb, tile);
+            int j, mb, tile, kp;
+            decode(i, j, mb, tile, kp);
             const int e = tl->touched[j];
-            const int p0 = a.off[e] + tile * kBN;
-            const int n_valid = min(kBN, tl->cnt[j] - tile * kBN);
+            const int p0 = a.off[e] + tile * tl->bnj[j];
+            const int n_valid = min(tl->bnj[j], tl->cnt[j] - tile * tl->bnj[j]);
             const int N = (n_valid + 15) & ~15;
             bool ok = !tl->abort_flag && mbar_wait_bounded(&tl->tfull, n_item & 1);
             if (!ok) {
@@ -397,71 +446,130 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 break;
             }
             tc_fence_after();
+            // rows of this thread: phase 0 gate/up row `ra`; phase 1 rows ra and ra + 128
+            const int ra = mb * rows_per_item + 32 * q + lane;
+            const int rb = a.phase == 0 ? ra : ra + kBM;
+            const bool va = ra < R, vb = rb < R;
+            float bg = 0.0f, bu = 0.0f;                 // biases of rows ra / rb (phase 1: b0 only)
             if (a.phase == 0) {
-                const int row = mb * kBM + 32 * q + lane;
-                const bool vr = row < R;
-                const size_t bi = static_cast<size_t>(e) * R + (vr ? row : 0);
-                const float bg = a.b0 ? __bfloat162float(__ushort_as_bfloat16(a.b0[bi])) : 0.0f;
-                const float bu = a.b1 ? __bfloat162float(__ushort_as_bfloat16(a.b1[bi])) : 0.0f;
-                uint16_t* hout = static_cast<uint16_t*>(a.out);
+                const size_t bi = static_cast<size_t>(e) * R + (va ? ra : 0);
+                if (a.b0) bg = __bfloat162float(__ushort_as_bfloat16(a.b0[bi]));
+                if (a.b1) bu = __bfloat162float(__ushort_as_bfloat16(a.b1[bi]));
+            } else if (a.b0) {
+                if (va) bg = __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + ra]));
+                if (vb) bu = __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + rb]));
+            }
+            uint16_t* hout = static_cast<uint16_t*>(a.out);
+            float* eout = static_cast<float*>(a.out);
+            if (S == 1) {
                 for (int c0 = 0; c0 < N; c0 += 16) {
-                    float g[16], u[16];
-                    tmem_ld16(tq + c0, g);
-                    tmem_ld16(tq + 256 + c0, u);
-                    unsigned hm[16];
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int c = c0 + t;
-                        hm[t] = 0u;
-                        if (vr && c < n_valid) {
-                            float gv = g[t], uv = u[t];
-                            if (QUANT) {
-                                const float inv = a.col_scale[p0 + c];
-                                gv *= inv;
-                                uv *= inv;
-                            }
-                            const float h = act_fn(a.act, gv + bg, uv + bu, a.limit, a.alpha);
-                            const uint16_t hb = float_to_adt_bits(h, a.adt);
-                            hout[static_cast<size_t>(p0 + c) * R + row] = hb;
-                            if (QUANT) hm[t] = __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt)));
-                        }
-                    }
-                    if (QUANT) {
-                        // per-route max |h| (positive floats order like their bit patterns):
-                        // reduced over the warp's 32 rows first, one atomic per warp and column
+                    float d0[16], d1[16];
+                    tmem_ld16_pair(tq + c0, tq + 256 + c0, d0, d1);
+                    if (a.phase == 0) {
+                        unsigned hm[16];
 #pragma unroll
                         for (int t = 0; t < 16; ++t) {
-                            const unsigned mv = __reduce_max_sync(0xffffffffu, hm[t]);
-                            if (lane == 0 && c0 + t < n_valid) atomicMax(a.hmax + p0 + c0 + t, mv);
+                            const int c = c0 + t;
+                            hm[t] = 0u;
+                            if (va && c < n_valid) {
+                                float gv = d0[t], uv = d1[t];
+                                if (QUANT) {
+                                    const float inv = a.col_scale[p0 + c];
+                                    gv *= inv;
+                                    uv *= inv;
+                                }
+                                const float h = act_fn(a.act, gv + bg, uv + bu, a.limit, a.alpha);
+                                const uint16_t hb = float_to_adt_bits(h, a.adt);
+                                hout[static_cast<size_t>(p0 + c) * R + ra] = hb;
+                                if (QUANT) hm[t] = __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt)));
+                            }
+                        }
+                        if (QUANT) {
+                            // per-route max |h| (positive floats order like their bit patterns):
+                            // reduced over the warp's 32 rows first, one atomic per warp and column
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) {
+                                const unsigned mv = __reduce_max_sync(0xffffffffu, hm[t]);
+                                if (lane == 0 && c0 + t < n_valid) atomicMax(a.hmax + p0 + c0 + t, mv);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const int c = c0 + t;
+                            if (c < n_valid) {
+                                const size_t r = static_cast<size_t>(a.perm[p0 + c]);
+                                const float inv = QUANT ? a.col_scale[p0 + c] : 1.0f;
+                                if (va) eout[r * R + ra] = d0[t] * inv + bg;
+                                if (vb) eout[r * R + rb] = d1[t] * inv + bu;
+                            }
                         }
                     }
                 }
-            } else {
-                const int row0 = mb * 2 * kBM + 32 * q + lane;
-                const int row1 = row0 + kBM;
-                const bool v0 = row0 < R, v1 = row1 < R;
-                const float b0 = (a.b0 && v0) ? __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + row0])) : 0.0f;
-                const float b1 = (a.b0 && v1) ? __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + row1])) : 0.0f;
-                float* eout = static_cast<float*>(a.out);
-                for (int c0 = 0; c0 < N; c0 += 16) {
-                    float d0[16], d1[16];
-                    tmem_ld16(tq + c0, d0);
-                    tmem_ld16(tq + 256 + c0, d1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tl->tempty);
+                continue;
+            }
+            // split K: park this part's accumulators, the group's last part finishes
+            float* part = a.part;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float d0[16], d1[16];
+                tmem_ld16_pair(tq + c0, tq + 256 + c0, d0, d1);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int c = c0 + t;
-                        if (c < n_valid) {
-                            const size_t r = static_cast<size_t>(a.perm[p0 + c]);
-                            const float inv = QUANT ? a.col_scale[p0 + c] : 1.0f;
-                            if (v0) eout[r * R + row0] = d0[t] * inv + b0;
-                            if (v1) eout[r * R + row1] = d1[t] * inv + b1;
-                        }
-                    }
+                for (int t = 0; t < 16; ++t) {
+                    const int c = c0 + t;
+                    if (c >= n_valid) continue;
+                    const size_t pr = (static_cast<size_t>(kp) * Tk + p0 + c) * 2;
+                    if (va) part[pr * R + ra] = d0[t];
+                    if (a.phase == 0 ? va : vb) part[(pr + 1) * R + (a.phase == 0 ? ra : rb)] = d1[t];
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tl->tempty);
+            if (lane == 0) mbar_arrive(&tl->tempty);     // TMEM is free again
+            // each warp owns its 32-row slice: one counter per (group, slice), so no barrier
+            // between the epilogue warps is needed
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                const int slot = (i / S) * 4 + q;
+                const int prev = atomicAdd(a.cnt + slot, 1);
+                last = (prev + 1 == S);
+                if (last) a.cnt[slot] = 0;               // ready for the next call
+            }
+            if (__shfl_sync(0xffffffffu, last, 0) == 0) continue;
+            __threadfence();
+            const int r1 = a.phase == 0 ? ra : rb;
+            const bool v1 = a.phase == 0 ? va : vb;
+            for (int c = 0; c < n_valid; ++c) {
+                // parts summed in K order
+                float x0 = 0.0f, x1 = 0.0f;
+                for (int kk = 0; kk < S; ++kk) {
+                    const size_t pr = (static_cast<size_t>(kk) * Tk + p0 + c) * 2;
+                    if (va) x0 += __ldcg(part + pr * R + ra);
+                    if (v1) x1 += __ldcg(part + (pr + 1) * R + r1);
+                }
+                const float inv = QUANT ? a.col_scale[p0 + c] : 1.0f;
+                if (a.phase == 0) {
+                    unsigned hm = 0u;
+                    if (va) {
+                        const float h = act_fn(a.act, x0 * inv + bg, x1 * inv + bu, a.limit, a.alpha);
+                        const uint16_t hb = float_to_adt_bits(h, a.adt);
+                        hout[static_cast<size_t>(p0 + c) * R + ra] = hb;
+                        hm = __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt)));
+                    }
+                    if (QUANT) {
+                        const unsigned mv = __reduce_max_sync(0xffffffffu, hm);
+                        if (lane == 0) atomicMax(a.hmax + p0 + c, mv);
+                    }
+                } else {
+                    const size_t r = static_cast<size_t>(a.perm[p0 + c]);
+                    if (va) eout[r * R + ra] = x0 * inv + bg;
+                    if (vb) eout[r * R + rb] = x1 * inv + bu;
+                }
+            }
         }
     }
     tc_fence_before();
@@ -604,8 +712,6 @@ bool make_map_2d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint
 
 }  // namespace
 
-size_t tc_gemm_smem_bytes() { return kStages * kStageQ + sizeof(SmemTail) + 1024; }
-
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
                                uint16_t* xs, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
@@ -627,12 +733,50 @@ cudaError_t launch_h_to_f16(const uint16_t* h, int adt, const unsigned* hmax, in
     return cudaGetLastError();
 }
 
+// Launch shape: routes per tile, ring depth and K split.  Decode-sized calls (few routes) use
+// 64-route tiles, a deep ring and, when the workspace has room for partials, split K so that the
+// few (expert, row block) tiles still spread over every SM.
+static TcLayout tc_layout(const GemmArgs& a, int num_sms, size_t* smem) {
+    TcLayout L{};
+    const int Tk = a.rows_in;
+    L.bn = Tk <= 256 ? 64 : 256;
+    const size_t tail = 4096 + 1024;
+    const size_t budget = 227 * 1024;
+    const int bbytes = (L.bn / 64) * kBBox;
+    if (a.quant) {
+        L.a_ring_bytes = 2 * 2 * kATile;
+        L.slot_bytes = (bbytes + kStaging + 1023) / 1024 * 1024;
+    } else {
+        L.a_ring_bytes = 0;
+        L.slot_bytes = 2 * kATile + bbytes;
+    }
+    L.nslot = static_cast<int>((budget - tail - L.a_ring_bytes) / L.slot_bytes);
+    if (L.nslot > kMaxSlots) L.nslot = kMaxSlots;
+    const int rows_per_item = a.phase == 0 ? kBM : 2 * kBM;
+    const int MB = (a.R + rows_per_item - 1) / rows_per_item;
+    const int nkb = a.K / kBK;
+    L.S = 1;
+    if (a.max_split > 1) {
+        const int e_eff = a.E < Tk ? a.E : Tk;
+        const long long tiles = static_cast<long long>(e_eff) * MB;
+        int S = static_cast<int>((4LL * num_sms + tiles - 1) / tiles);
+        if (S > a.max_split) S = a.max_split;
+        if (S > nkb / 4) S = nkb / 4;
+        L.S = S < 1 ? 1 : S;
+    }
+    *smem = 1024 + L.a_ring_bytes + static_cast<size_t>(L.nslot) * L.slot_bytes + 4096;
+    return L;
+}
+
 cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     TcParams P;
     memset(&P, 0, sizeof(P));
     P.a = a;
     const int KA = a.K;                 // reduction length
     const int Rm = a.R;                 // rows per expert matrix
+    size_t smem = 0;
+    P.ly = tc_layout(a, num_sms, &smem);
+    if (P.ly.nslot < 2) return cudaErrorInvalidValue;
     if (!a.quant) {
         if (!make_map_3d(&P.tmA0, a.w0, a.ab_bf16, KA, Rm, a.E, kBM)) return cudaErrorInvalidValue;
         if (!make_map_3d(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, a.ab_bf16, KA, Rm, a.E, kBM))
@@ -645,12 +789,10 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     if (!make_map_2d(&P.tmB, a.act_in, a.ab_bf16, KA, a.rows_in, 64)) return cudaErrorInvalidValue;
     cudaError_t e;
     if (a.quant) {
-        const size_t smem = kStages * kStageQ + sizeof(SmemTail) + 1024;
         e = ensure_smem(tc_gemm_kernel<true>, smem);
         if (e != cudaSuccess) return e;
         tc_gemm_kernel<true><<<num_sms, kThreadsQ, smem, s>>>(P);
     } else {
-        const size_t smem = kStages * kStage + sizeof(SmemTail) + 1024;
         e = ensure_smem(tc_gemm_kernel<false>, smem);
         if (e != cudaSuccess) return e;
         tc_gemm_kernel<false><<<num_sms, kThreads, smem, s>>>(P);

@@ -166,6 +166,113 @@ __device__ __forceinline__ void decode_unit(int u, int RT, const int* goff, int 
     g = local % ng;
 }
 
+// Stages one activation row into shared memory in the mma operand type: f16 with a
+// power-of-two prescale (max |x| * 2^ks in [2^14, 2^15)) when bf16 activations feed the f16
+// mma, else the bits as they are; element order inside each 8-group is natural, or
+// (0,4,1,5,2,6,3,7) for INT4.  For K <= 3072 the row is read once, with every load issued
+// before any is used; returns the inverse prescale.
+template <int FMT>
+__device__ __forceinline__ float stage_row(const uint16_t* __restrict__ src, unsigned char* xrow,
+                                           float* xsum, int col, int K, int nblk, bool prescale,
+                                           bool copy_bits, int lane) {
+    auto store_block = [&](int blk, const uint32_t (&wv)[16], float scl) {
+        uint16_t o[32];
+        float bsum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const uint16_t bits = static_cast<uint16_t>((q & 1) ? (wv[q >> 1] >> 16) : (wv[q >> 1] & 0xFFFF));
+            uint16_t ob;
+            if (copy_bits) {
+                ob = bits;
+            } else {
+                const float v = __fmul_rn(__bfloat162float(__ushort_as_bfloat16(bits)), scl);
+                ob = __half_as_ushort(__float2half_rn(v));
+            }
+            if (FMT == FMT_INT4) bsum += __half2float(__ushort_as_half(ob));
+            o[q] = ob;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+#pragma unroll
+            for (int pr = 0; pr < 4; ++pr) {
+                uint16_t lo, hi;
+                if (FMT == FMT_INT4) { lo = o[q8 * 8 + pr]; hi = o[q8 * 8 + pr + 4]; }
+                else { lo = o[q8 * 8 + 2 * pr]; hi = o[q8 * 8 + 2 * pr + 1]; }
+                pk[q8 * 4 + pr] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(xrow + static_cast<size_t>(blk) * 64);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) d4[h] = make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+        if (FMT == FMT_INT4) xsum[blk * 8 + col] = bsum;
+    };
+    auto absmax16 = [&](const uint32_t (&wv)[16]) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+            mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(wv[h] & 0xFFFF))));
+            mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(wv[h] >> 16))));
+        }
+        return mx;
+    };
+    auto prescale_of = [&](float mx, float& scl, float& inv) {
+        scl = inv = 1.0f;
+        if (mx > 0.0f && mx < 3.0e38f) {
+            int ex;
+            frexpf(mx, &ex);            // mx = f * 2^ex, f in [0.5, 1)
+            const int ks = max(-120, min(120, 15 - ex));
+            scl = __uint_as_float(static_cast<uint32_t>(ks + 127) << 23);
+            inv = __uint_as_float(static_cast<uint32_t>(127 - ks) << 23);
+        }
+    };
+    float scl = 1.0f, inv = 1.0f;
+    if (nblk <= 96) {
+        uint32_t wv[3][16];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int blk = lane + 32 * q;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (blk < nblk) v = __ldg(reinterpret_cast<const uint4*>(src + blk * kBlockK) + h);
+                wv[q][4 * h] = v.x; wv[q][4 * h + 1] = v.y; wv[q][4 * h + 2] = v.z; wv[q][4 * h + 3] = v.w;
+            }
+        }
+        if (prescale) {
+            float mx = fmaxf(fmaxf(absmax16(wv[0]), absmax16(wv[1])), absmax16(wv[2]));
+            prescale_of(warp_max(mx), scl, inv);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q)
+            if (lane + 32 * q < nblk) store_block(lane + 32 * q, wv[q], scl);
+        return inv;
+    }
+    if (prescale) {
+        float mx = 0.0f;
+        for (int blk = lane; blk < nblk; blk += 32) {
+            uint32_t wv[16];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + blk * kBlockK) + h);
+                wv[4 * h] = v.x; wv[4 * h + 1] = v.y; wv[4 * h + 2] = v.z; wv[4 * h + 3] = v.w;
+            }
+            mx = fmaxf(mx, absmax16(wv));
+        }
+        prescale_of(warp_max(mx), scl, inv);
+    }
+    for (int blk = lane; blk < nblk; blk += 32) {
+        uint32_t wv[16];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + blk * kBlockK) + h);
+            wv[4 * h] = v.x; wv[4 * h + 1] = v.y; wv[4 * h + 2] = v.z; wv[4 * h + 3] = v.w;
+        }
+        store_block(blk, wv, scl);
+    }
+    return inv;
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ KParams P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -388,10 +495,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
     // ================================== consumer warps =========================================
     const int gid = lane >> 2, tid = lane & 3;
-    const int brow = gid < tg ? gid : 0;   // activation row this lane feeds to the mma
     int it = 0, j = 0;
     int staged_j = -1, staged_g = -1;
     const uint16_t* in = a.in;
+    const bool copy_bits = kMmaBf16 || a.adt == 0;
+    // Phase 1 with at most tg tokens: every token's row is staged once here (x is per token and
+    // shared by every expert), and the units index it by token; otherwise rows are staged per
+    // group of routes when the group changes.
+    const bool tokmode = a.phase == 0 && a.T <= tg;
+    if (tokmode) {
+        if (warp < 8) {
+            const int t = warp;
+            float inv = 0.0f;
+            if (t < a.T) {
+                inv = stage_row<FMT>(in + static_cast<size_t>(t) * K, c.xs + static_cast<size_t>(t) * p.xstride,
+                                     c.xsum, t, K, nblk, prescale, copy_bits, lane);
+            } else if (FMT == FMT_INT4) {
+                for (int blk = lane; blk < nblk; blk += 32) c.xsum[blk * 8 + t] = 0.0f;
+            }
+            if (lane == 0) c.xinv[t] = inv;
+        }
+        named_bar(1, kNCW * 32);
+    }
 
     for (int u = u0; u < u1; ++u) {
         int rt, g;
@@ -399,9 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         const int e = c.touched[j];
         const int cnt_g = min(tg, c.cnt[j] - g * tg);
         const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
+        // staged row of each of the unit's columns (routes): the token in token mode
+        auto row_of = [&](int n) {
+            if (!tokmode) return n < tg ? n : 0;
+            if (n >= cnt_g) return 0;
+            return a.dense ? rbase + n : PERM[rbase + n] / a.k;
+        };
+        const int brow = row_of(gid);                 // activation row this lane feeds the mma
+        const int xc0 = row_of(2 * tid), xc1 = row_of(2 * tid + 1);   // INT4 x-sum columns
 
         // ---- stage this group's activations (f16 with prescale, or as-is) -----------------
-        if (j != staged_j || g != staged_g) {
+        if (!tokmode && (j != staged_j || g != staged_g)) {
             // every compute warp must be done with the previous group's activations
             if (staged_j >= 0) named_bar(1, kNCW * 32);
             staged_j = j;
@@ -414,72 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     size_t row;
                     if (a.phase == 0) row = a.dense ? static_cast<size_t>(rid) : static_cast<size_t>(rid / a.k);
                     else row = static_cast<size_t>(rid);
-                    const uint16_t* src = in + row * K;
-                    float scl = 1.0f;
-                    inv = 1.0f;
-                    if (prescale) {
-                        float mx = 0.0f;
-                        for (int q = lane; q < K / 8; q += 32) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(src + q * 8);
-                            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(w4[h] & 0xFFFF))));
-                                mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(w4[h] >> 16))));
-                            }
-                        }
-                        mx = warp_max(mx);
-                        if (mx > 0.0f && mx < 3.0e38f) {
-                            int ex;
-                            frexpf(mx, &ex);            // mx = f * 2^ex, f in [0.5, 1)
-                            int ks = 15 - ex;           // mx * 2^ks in [2^14, 2^15)
-                            ks = max(-120, min(120, ks));
-                            scl = __uint_as_float(static_cast<uint32_t>(ks + 127) << 23);
-                            inv = __uint_as_float(static_cast<uint32_t>(127 - ks) << 23);
-                        }
-                    }
-                    unsigned char* xrow = c.xs + static_cast<size_t>(n) * p.xstride;
-                    for (int blk = lane; blk < nblk; blk += 32) {
-                        uint32_t wv[16];
-                        const uint4* s4 = reinterpret_cast<const uint4*>(src + blk * kBlockK);
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const uint4 v = s4[h];
-                            wv[4 * h + 0] = v.x; wv[4 * h + 1] = v.y; wv[4 * h + 2] = v.z; wv[4 * h + 3] = v.w;
-                        }
-                        uint16_t o[32];
-                        float bsum = 0.0f;
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const uint16_t bits = static_cast<uint16_t>((q & 1) ? (wv[q >> 1] >> 16) : (wv[q >> 1] & 0xFFFF));
-                            uint16_t ob;
-                            if (kMmaBf16 || a.adt == 0) {
-                                ob = bits;
-                                if (FMT == FMT_INT4) bsum += __half2float(__ushort_as_half(ob));
-                            } else {
-                                const float v = __fmul_rn(__bfloat162float(__ushort_as_bfloat16(bits)), scl);
-                                ob = __half_as_ushort(__float2half_rn(v));
-                                if (FMT == FMT_INT4) bsum += __half2float(__ushort_as_half(ob));
-                            }
-                            o[q] = ob;
-                        }
-                        // element order inside each 8-group: natural, or (0,4,1,5,2,6,3,7) for INT4
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-#pragma unroll
-                            for (int pr = 0; pr < 4; ++pr) {
-                                uint16_t lo, hi;
-                                if (FMT == FMT_INT4) { lo = o[q8 * 8 + pr]; hi = o[q8 * 8 + pr + 4]; }
-                                else { lo = o[q8 * 8 + 2 * pr]; hi = o[q8 * 8 + 2 * pr + 1]; }
-                                pk[q8 * 4 + pr] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-                            }
-                        }
-                        uint4* d4 = reinterpret_cast<uint4*>(xrow + static_cast<size_t>(blk) * 64);
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) d4[h] = make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
-                        if (FMT == FMT_INT4) c.xsum[blk * 8 + n] = bsum;
-                    }
+                    inv = stage_row<FMT>(in + row * K, c.xs + static_cast<size_t>(n) * p.xstride, c.xsum, n,
+                                         K, nblk, prescale, copy_bits, lane);
                 } else {
                     if (n < tg) {
                         unsigned char* xrow = c.xs + static_cast<size_t>(n) * p.xstride;
@@ -538,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                             const unsigned char* blk = st + static_cast<size_t>(i) * BB;
                             const uint2 cw = *reinterpret_cast<const uint2*>(blk + lane * 8);
                             const uint2 smv = *reinterpret_cast<const uint2*>(blk + 256 + gid * 8);
-                            const float2 xsm = *reinterpret_cast<const float2*>(c.xsum + (b0 + i) * 8 + 2 * tid);
+                            const float2 xsm = make_float2(c.xsum[(b0 + i) * 8 + xc0], c.xsum[(b0 + i) * 8 + xc1]);
                             float d[4] = {0.f, 0.f, 0.f, 0.f};
                             mma_f16_16816(d, u4pair_to_f16x2(cw.x, 0), u4pair_to_f16x2(cw.y, 0),
                                           u4pair_to_f16x2(cw.x, 4), u4pair_to_f16x2(cw.y, 4), bx.x, bx.y);
@@ -603,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 rm[(gid + 8) * 8 + 2 * tid] = acc[m][2];
                 rm[(gid + 8) * 8 + 2 * tid + 1] = acc[m][3];
             }
-            if (warp == 0 && lane < 8) c.rinv[b * 8 + lane] = c.xinv[lane];
+            if (warp == 0 && lane < 8) c.rinv[b * 8 + lane] = c.xinv[row_of(lane)];
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.rfull[b]);
         }

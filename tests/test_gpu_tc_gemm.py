@@ -36,6 +36,9 @@ CASES = [
     (2, 40, dict(H=512, I=384, E=8, k=4)),            # MXFP4 + clamped SwiGLU + biases
     (3, 77, dict(H=640, I=448, E=8, k=4)),            # MXFP4, skewed, partial 128-row blocks
     (3, 512, None),                                   # full gpt-oss prefill micro-batch
+    (2, 1, None),                                     # gpt-oss decode T=1 (split K)
+    (2, 8, None),                                     # gpt-oss decode T=8 (split K)
+    (5, 8, dict(H=4096, I=14336, E=8, k=2)),          # Mixtral decode through the tensor cores
 ]
 
 
@@ -65,7 +68,7 @@ def test_tc_gemm_parity(case):
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
     oex, _ = oracle_layer(L)
-    toks = None if T <= 48 else np.unique(np.linspace(0, T - 1, 6).astype(np.int32))
+    toks = None if (T <= 48 and shapes is not None) else np.unique(np.linspace(0, T - 1, 6).astype(np.int32))
     oy, oy32, _ = oracle.moe_forward(xb, c["adt"], oex, oidx, ow, tokens=toks, nthreads=NTHREADS)
     rows = slice(None) if toks is None else toks
     fb = None
@@ -118,3 +121,51 @@ def test_gemm_path_refuses_int4_weights():
     with pytest.raises(moe.TsMoeError) as ei:
         moe.forward(D["x"], ex, idx, w, path="gemm")
     assert ei.value.status == 2
+
+
+def _widen_scales(L, lo, hi, frac, seed):
+    """Replace a random `frac` of the MXFP4 block exponents of every matrix by values in [lo, hi]."""
+    g = torch.Generator().manual_seed(seed)
+    for name in ("gate_s", "up_s", "down_s"):
+        s = L["experts"][name]
+        pick = torch.rand(s.shape, generator=g) < frac
+        s[pick] = torch.randint(lo, hi + 1, (int(pick.sum()),), generator=g).to(torch.uint8)
+
+
+def test_tc_gemm_mxfp4_scales_outside_normal_f16():
+    # block scales 2^-23 .. 2^1: below 2^-14 the scale itself is not a normal f16 number, yet
+    # every scaled e2m1 value still is an exact f16 number, so the result must match the oracle
+    moe = _moe()
+    L = synth.make_layer(2, T=24, shapes=dict(H=256, I=192, E=4, k=2), device="cpu")
+    _widen_scales(L, 104, 128, 0.1, 11)
+    D = to_device(L, "cuda")
+    c = L["cfg"]
+    xb = bits16(L["x"])
+    _, _, oidx, ow = oracle_route(L, xb)
+    ex, _ = gpu_layer(D)
+    ws = moe.alloc_workspace(24, c["k"], ex)
+    y, y32 = moe.forward(D["x"], ex, torch.from_numpy(oidx).cuda(), torch.from_numpy(ow).cuda(),
+                         want_f32=True, ws=ws, path="gemm")
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
+    oex, _ = oracle_layer(L)
+    oy, oy32, _ = oracle.moe_forward(xb, c["adt"], oex, oidx, ow, nthreads=NTHREADS)
+    check_outputs(oracle.adt_bits_to_f64(bits16(y), c["adt"]), y32.double().cpu().numpy(),
+                  oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"])
+
+
+def test_tc_gemm_reports_scales_it_cannot_represent():
+    # a block scale of 2^-27: its scaled e2m1 values are not all f16 numbers; the tensor-core
+    # path must say so through the device status (the GEMV path computes such layers exactly)
+    moe = _moe()
+    L = synth.make_layer(2, T=24, shapes=dict(H=256, I=192, E=4, k=2), device="cpu")
+    L["experts"]["gate_s"][1, 3, 2] = 100
+    D = to_device(L, "cuda")
+    c = L["cfg"]
+    ex, _ = gpu_layer(D)
+    idx = torch.tensor([[1, 2]] * 24, dtype=torch.int32, device="cuda")
+    w = torch.full((24, 2), 0.5, dtype=torch.float32, device="cuda")
+    ws = moe.alloc_workspace(24, c["k"], ex)
+    moe.forward(D["x"], ex, idx, w, ws=ws, path="gemm")
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 2
