@@ -190,6 +190,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     SmemTail* tl = reinterpret_cast<SmemTail*>(ring + static_cast<size_t>(Ly.nslot) * Ly.slot_bytes);
     const GemmArgs& a = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();                 // inputs of this launch may come from the previous kernel
+    pdl_launch_dependents();
     const int R = a.R, K = a.K;
     const int rows_per_item = a.phase == 0 ? kBM : 2 * kBM;
     const int MB = (R + rows_per_item - 1) / rows_per_item;
@@ -584,6 +586,8 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ perm,
                                                           int k, int H, int n,
                                                           uint16_t* __restrict__ xs) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int p = blockIdx.x;
     if (p >= n) return;
     const int t = perm[p] / k;
@@ -621,6 +625,8 @@ __global__ void __launch_bounds__(128) gather_rows_f16_kernel(const uint16_t* __
                                                               float* __restrict__ inv_out,
                                                               unsigned* __restrict__ hmax) {
     __shared__ float red[4];
+    pdl_wait();
+    pdl_launch_dependents();
     const int p = blockIdx.x;
     if (p >= n) return;
     const uint16_t* src = x + static_cast<size_t>(perm[p] / k) * H;
@@ -643,6 +649,8 @@ __global__ void __launch_bounds__(128) h_to_f16_kernel(const uint16_t* __restric
                                                        const unsigned* __restrict__ hmax, int I, int n,
                                                        uint16_t* __restrict__ h16,
                                                        float* __restrict__ inv_out) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int p = blockIdx.x;
     if (p >= n) return;
     float scl, inv;
@@ -715,22 +723,19 @@ bool make_map_2d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
                                uint16_t* xs, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    gather_rows_kernel<<<n, 128, 0, s>>>(x, perm, k, H, n, xs);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(n), dim3(128), 0, s, x, perm, k, H, n, xs);
 }
 
 cudaError_t launch_gather_rows_f16(const uint16_t* x, int adt, const int32_t* perm, int k, int H,
                                    int n, uint16_t* xs, float* inv, unsigned* hmax, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    gather_rows_f16_kernel<<<n, 128, 0, s>>>(x, adt, perm, k, H, n, xs, inv, hmax);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_f16_kernel, dim3(n), dim3(128), 0, s, x, adt, perm, k, H, n, xs, inv, hmax);
 }
 
 cudaError_t launch_h_to_f16(const uint16_t* h, int adt, const unsigned* hmax, int I, int n,
                             uint16_t* h16, float* inv, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    h_to_f16_kernel<<<n, 128, 0, s>>>(h, adt, hmax, I, n, h16, inv);
-    return cudaGetLastError();
+    return launch_pdl(h_to_f16_kernel, dim3(n), dim3(128), 0, s, h, adt, hmax, I, n, h16, inv);
 }
 
 // Launch shape: routes per tile, ring depth and K split.  Decode-sized calls (few routes) use
@@ -791,11 +796,11 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     if (a.quant) {
         e = ensure_smem(tc_gemm_kernel<true>, smem);
         if (e != cudaSuccess) return e;
-        tc_gemm_kernel<true><<<num_sms, kThreadsQ, smem, s>>>(P);
+        return launch_pdl(tc_gemm_kernel<true>, dim3(num_sms), dim3(kThreadsQ), smem, s, P);
     } else {
         e = ensure_smem(tc_gemm_kernel<false>, smem);
         if (e != cudaSuccess) return e;
-        tc_gemm_kernel<false><<<num_sms, kThreads, smem, s>>>(P);
+        return launch_pdl(tc_gemm_kernel<false>, dim3(num_sms), dim3(kThreads), smem, s, P);
     }
     return cudaGetLastError();
 }

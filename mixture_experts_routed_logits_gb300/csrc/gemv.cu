@@ -73,7 +73,8 @@ __host__ inline Plan make_plan(int fmt, int K, int tg_cap) {
                          + (3 * kMaxExperts + 1 + 8) * 4                     // unit tables
                          + 2 * 8 * 4 + 4 * 8                                 // reducer hand-off
                          + (kMaxExperts + 1 + kMaxLocalRoutes) * 4            // in-kernel routes
-                         + 16 * 16;                                           // region padding
+                         + 32 * 4                                            // combine tile list
+                         + 17 * 16;                                           // region padding
     for (int ns = kMaxStages; ns >= 2; --ns) {
         const size_t ring = static_cast<size_t>(ns) * kStageBytes;
         if (ring + fixed >= static_cast<size_t>(kSmemBudget)) continue;
@@ -108,12 +109,13 @@ struct Carve {
     int* touched;     // [256]
     int* cnt;         // [256]
     int* goff;        // [257]
-    int* misc;        // [8]: 0 = ntouched, 1 = abort flag
+    int* misc;        // [8]: 0 = ntouched, 1 = abort flag, 2 = combine on, 3 = tiles this round
     float* rinv;      // [2][8]: prescale inverses travelling with the partials
     uint64_t* rfull;  // [2]: partials of a unit written (16 compute warps arrive)
     uint64_t* rempty; // [2]: partial buffer read by the reducer
     int* off_s;       // [257]: route offsets built in the kernel
     int* perm_s;      // [512]: route list built in the kernel
+    int* ctile;       // [32]: row tiles this CTA combines in the current round
 };
 
 __device__ inline Carve carve(unsigned char* base, const Plan& p, int K) {
@@ -141,6 +143,7 @@ __device__ inline Carve carve(unsigned char* base, const Plan& p, int K) {
     c.rinv = reinterpret_cast<float*>(take(2 * 8 * 4));
     c.off_s = reinterpret_cast<int*>(take((kMaxExperts + 1) * 4));
     c.perm_s = reinterpret_cast<int*>(take(kMaxLocalRoutes * 4));
+    c.ctile = reinterpret_cast<int*>(take(32 * 4));
     return c;
 }
 
@@ -291,6 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
     Carve c = carve(smem_raw, p, K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();                 // inputs of this launch may come from the previous kernel
+    pdl_launch_dependents();
 
     // ---- route list (built here for decode sizes), unit tables --------------------------------
     const int* OFF = a.off;
@@ -299,54 +304,137 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         OFF = c.off_s;
         PERM = c.perm_s;
     }
-    if (threadIdx.x == 0) {
+    // Phase 1 with at most tg tokens ("token mode"): every token's row is staged once (x is per
+    // token and shared by every expert) and the units index it by token; otherwise rows are
+    // staged per group of routes when the group changes.
+    const bool tokmode = a.phase == 0 && a.T <= tg;
+    const bool copy_bits = kMmaBf16 || a.adt == 0;
+    if (warp == kNCW + 1) {
+        // ---- route list (decode sizes) and unit tables, built by one warp --------------------
         if (a.idx) {
-            // counting sort of the route ids by expert, ascending id inside an expert
+            // counting sort of the route ids by expert, ascending id inside an expert: chunks of
+            // 32 routes, experts of a chunk grouped with match_any, one counter update per group
             const int n = a.T * a.k;
-            for (int e = 0; e <= a.E; ++e) c.off_s[e] = 0;
-            for (int r = 0; r < n; ++r) {
-                const int e = a.idx[r];
-                if (e >= 0 && e < a.E) c.off_s[e + 1] += 1;
-                else report_error(a.status, DEV_ERR_INVALID);
+            int ev[kMaxLocalRoutes / 32];
+#pragma unroll
+            for (int q = 0; q < kMaxLocalRoutes / 32; ++q) {
+                const int r = q * 32 + lane;
+                ev[q] = r < n ? a.idx[r] : -1;
             }
-            for (int e = 0; e < a.E; ++e) c.off_s[e + 1] += c.off_s[e];
-            for (int e = 0; e < a.E; ++e) c.cnt[e] = c.off_s[e];     // cursors (cnt reused)
-            for (int r = 0; r < n; ++r) {
-                const int e = a.idx[r];
-                if (e >= 0 && e < a.E) c.perm_s[c.cnt[e]++] = r;
+            for (int e = lane; e <= a.E; e += 32) c.off_s[e] = 0;
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < kMaxLocalRoutes / 32; ++q) {
+                if (q * 32 >= n) break;
+                const int r = q * 32 + lane;
+                const bool valid = ev[q] >= 0 && ev[q] < a.E;
+                if (r < n && !valid) report_error(a.status, DEV_ERR_INVALID);
+                const unsigned peers = __match_any_sync(0xffffffffu, valid ? ev[q] : -1);
+                if (valid && __ffs(peers) - 1 == lane) c.off_s[ev[q] + 1] += __popc(peers);
+                __syncwarp();
+            }
+            // inclusive scan of the counts (off_s[1..E]) -> route offsets; lane l owns 8 entries
+            {
+                int loc[8], sum = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = lane * 8 + q;
+                    loc[q] = e < a.E ? c.off_s[e + 1] : 0;
+                    sum += loc[q];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += v;
+                }
+                int run = incl - sum;
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int e = lane * 8 + q;
+                    run += loc[q];
+                    if (e < a.E) {
+                        c.off_s[e + 1] = run;
+                        c.cnt[e] = run - loc[q];          // placement cursor (cnt reused)
+                    }
+                }
+                __syncwarp();
+            }
+#pragma unroll
+            for (int q = 0; q < kMaxLocalRoutes / 32; ++q) {
+                if (q * 32 >= n) break;
+                const int r = q * 32 + lane;
+                const bool valid = ev[q] >= 0 && ev[q] < a.E;
+                const unsigned peers = __match_any_sync(0xffffffffu, valid ? ev[q] : -1);
+                if (valid) c.perm_s[c.cnt[ev[q]] + __popc(peers & ((1u << lane) - 1u))] = r;
+                __syncwarp();
+                if (valid && __ffs(peers) - 1 == lane) c.cnt[ev[q]] += __popc(peers);
+                __syncwarp();
             }
         }
+        // touched experts in ascending order with their route counts and group prefix
         int nt = 0, acc = 0;
         if (a.dense) {
-            c.touched[0] = 0;
-            c.cnt[0] = a.T;
-            c.goff[0] = 0;
+            if (lane == 0) {
+                c.touched[0] = 0;
+                c.cnt[0] = a.T;
+                c.goff[0] = 0;
+            }
             acc = (a.T + tg - 1) / tg;
             nt = 1;
         } else {
-            for (int e = 0; e < a.E; ++e) {
-                const int n = OFF[e + 1] - OFF[e];
-                if (n > 0) {
-                    c.touched[nt] = e;
-                    c.cnt[nt] = n;
-                    c.goff[nt] = acc;
-                    acc += (n + tg - 1) / tg;
-                    ++nt;
+            for (int e0 = 0; e0 < a.E; e0 += 32) {
+                const int e = e0 + lane;
+                const int n = e < a.E ? OFF[e + 1] - OFF[e] : 0;
+                const unsigned m = __ballot_sync(0xffffffffu, n > 0);
+                const int groups = n > 0 ? (n + tg - 1) / tg : 0;
+                int incl = groups;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += v;
                 }
+                __syncwarp();
+                if (n > 0) {
+                    const int pos = nt + __popc(m & ((1u << lane) - 1u));
+                    c.touched[pos] = e;
+                    c.cnt[pos] = n;
+                    c.goff[pos] = acc + incl - groups;
+                }
+                __syncwarp();
+                acc += __shfl_sync(0xffffffffu, incl, 31);
+                nt += __popc(m);
             }
         }
-        c.goff[nt] = acc;
-        c.misc[0] = nt;
-        c.misc[1] = 0;
-        for (int s = 0; s < p.nstages; ++s) {
-            mbar_init(&c.full[s], 1);
-            mbar_init(&c.empty[s], kNCW);
+        if (lane == 0) {
+            c.goff[nt] = acc;
+            c.misc[0] = nt;
+            c.misc[1] = 0;
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&c.rfull[b], kNCW);
-            mbar_init(&c.rempty[b], 1);
+    } else if (warp == kNCW) {
+        if (lane == 0) {
+            for (int s = 0; s < p.nstages; ++s) {
+                mbar_init(&c.full[s], 1);
+                mbar_init(&c.empty[s], kNCW);
+            }
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&c.rfull[b], kNCW);
+                mbar_init(&c.rempty[b], 1);
+            }
+            fence_mbar_init();
         }
-        fence_mbar_init();
+    } else if (tokmode && warp < 8) {
+        // token mode: stage every token's row while the route tables are being built
+        const int t = warp;
+        float inv = 0.0f;
+        if (t < a.T) {
+            inv = stage_row<FMT>(a.in + static_cast<size_t>(t) * K, c.xs + static_cast<size_t>(t) * p.xstride,
+                                 c.xsum, t, K, nblk, prescale, copy_bits, lane);
+        } else if (FMT == FMT_INT4) {
+            for (int blk = lane; blk < nblk; blk += 32) c.xsum[blk * 8 + t] = 0.0f;
+        }
+        if (lane == 0) c.xinv[t] = inv;
     }
     // the phase-1 launch clears the combine counters the phase-2 launch will count with
     if (a.cmb_mode == 1 && blockIdx.x == 0)
@@ -358,19 +446,92 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int u1 = static_cast<int>((static_cast<long long>(U) * (blockIdx.x + 1)) / gridDim.x);
     if (u0 >= u1) return;
 
+    // Fused combine (phase 2 of a routed decode call), run by the compute warps and the
+    // reducer warp together once every unit of this CTA is stored: every unit bumps its 16-row
+    // tile's counter (over all CTAs); the CTA that completes a tile's count runs the
+    // slot-ordered combine of that tile.  Rounds of up to 32 units: the reducer bumps 32
+    // counters at once (one lane each) and lists the completed tiles, then all 17 warps
+    // combine them.
+    auto fused_combine = [&]() {
+        constexpr int kCmbThreads = (kNCW + 1) * 32;
+        named_bar(2, kCmbThreads);                  // combine decision published
+        if (!c.misc[2]) return;
+        const int tix = warp < kNCW ? threadIdx.x : kNCW * 32 + lane;
+        const int per = a.T * kRowTile;
+        const float* ev = static_cast<const float*>(a.out);
+        int jl = 0;
+        for (int ub = u0; ub < u1; ub += 32) {
+            if (warp == kNCW + 1) {
+                const int u = ub + lane;
+                int rt = 0, last = 0;
+                if (u < u1) {
+                    int g;
+                    decode_unit(u, RT, c.goff, nt, jl, rt, g, c.cnt, tg);
+                    last = atomicAdd(a.cmb_cnt + rt, 1) + 1 == c.goff[nt];
+                }
+                const unsigned lm = __ballot_sync(0xffffffffu, last);
+                if (last) {
+                    c.ctile[__popc(lm & ((1u << lane) - 1u))] = rt;
+                    a.cmb_cnt[rt] = 0;                  // complete: ready for the next call
+                }
+                if (lane == 0) c.misc[3] = __popc(lm);
+                if (lm) __threadfence();
+            }
+            named_bar(2, kCmbThreads);              // tile list ready
+            const int ntile = c.misc[3];
+            for (int o = tix; o < ntile * per; o += kCmbThreads) {
+                const int tile = o / per, rem = o - tile * per;
+                const int t = rem / kRowTile, orow = c.ctile[tile] * kRowTile + rem % kRowTile;
+                const size_t yo = static_cast<size_t>(t) * R + orow;
+                float accv = a.seed ? __ldcg(a.seed + yo) : 0.0f;
+                // products fetched four slots at a time, added in slot order
+                for (int q0 = 0; q0 < a.k; q0 += 4) {
+                    float pv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const size_t r = static_cast<size_t>(t) * a.k + q0 + q;
+                        pv[q] = q0 + q < a.k ? __fmul_rn(a.w[r], __ldcg(ev + r * R + orow)) : 0.0f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q0 + q < a.k) accv = __fadd_rn(accv, pv[q]);
+                }
+                if (a.y_f32) a.y_f32[yo] = accv;
+                static_cast<uint16_t*>(a.y)[yo] = float_to_adt_bits(accv, a.adt);
+            }
+            named_bar(2, kCmbThreads);              // tile list consumed
+        }
+    };
+
     if (warp == kNCW + 1) {
         // ================================ reducer warp ======================================
         // Sums the 16 compute warps' partials of each unit in fixed warp order, applies the
         // prescale inverse, bias and activation, stores the unit's outputs; in phase 2 of a
         // routed decode call the last unit of each 16-row tile also runs the slot-ordered
-        // combine for that tile.
-        int j = 0;
+        // combine for that tile.  Every output this lane touches has row (lane & 15) of the
+        // tile, so the unit's biases are fetched one unit ahead (lane l < 16: bias 0 of row l,
+        // lane 16 + l: bias 1) and handed out with shuffles.
+        const int row = lane & 15;
+        int j = 0, jb = 0;
+        auto fetch_bias = [&](int u) {
+            int rt_, g_;
+            decode_unit(u, RT, c.goff, nt, jb, rt_, g_, c.cnt, tg);
+            const uint16_t* bp = lane < 16 ? a.b0 : (a.phase == 0 ? a.b1 : nullptr);
+            if (!bp) return 0.0f;
+            return __bfloat162float(__ushort_as_bfloat16(
+                bp[static_cast<size_t>(c.touched[jb]) * R + rt_ * kRowTile + row]));
+        };
+        float bias_next = fetch_bias(u0);
         for (int u = u0; u < u1; ++u) {
             int rt, g;
             decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
             const int e = c.touched[j];
             const int cnt_g = min(tg, c.cnt[j] - g * tg);
             const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
+            const float bias_cur = bias_next;
+            if (u + 1 < u1) bias_next = fetch_bias(u + 1);
+            const float bias0 = __shfl_sync(0xffffffffu, bias_cur, row);
+            const float bias1 = __shfl_sync(0xffffffffu, bias_cur, 16 + row);
             const int nl = u - u0, b = nl & 1;
             const bool ok = c.misc[1] == 0 && mbar_wait_bounded(&c.rfull[b], (nl >> 1) & 1);
             if (!ok) {
@@ -380,23 +541,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 }
             } else {
                 const float* redb = c.red + static_cast<size_t>(b) * kNCW * 2 * kRowTile * 8;
-                for (int o = lane; o < kRowTile * 8; o += 32) {
-                    const int n = o / kRowTile, row = o % kRowTile;
-                    if (n >= cnt_g) continue;
+                const int orow = rt * kRowTile + row;
+                for (int n = lane >> 4; n < cnt_g; n += 2) {
                     const int rid = a.dense ? rbase + n : PERM[rbase + n];
-                    const int orow = rt * kRowTile + row;
                     float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
                     for (int w = 0; w < kNCW; ++w) {
                         s0 += redb[(w * 2 + 0) * kRowTile * 8 + row * 8 + n];
                         if (nmat == 2) s1 += redb[(w * 2 + 1) * kRowTile * 8 + row * 8 + n];
                     }
                     const float inv = c.rinv[b * 8 + n];
-                    s0 *= inv;
-                    s1 *= inv;
-                    const size_t bidx = static_cast<size_t>(e) * R + orow;
-                    if (a.b0) s0 += __bfloat162float(__ushort_as_bfloat16(a.b0[bidx]));
+                    s0 = s0 * inv + bias0;
                     if (a.phase == 0) {
-                        if (a.b1) s1 += __bfloat162float(__ushort_as_bfloat16(a.b1[bidx]));
+                        s1 = s1 * inv + bias1;
                         const float h = act_fn(a.act, s0, s1, a.limit, a.alpha);
                         static_cast<uint16_t*>(a.out)[static_cast<size_t>(rid) * R + orow] = float_to_adt_bits(h, a.adt);
                     } else {
@@ -407,35 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.rempty[b]);
         }
-        if (a.cmb_mode == 2 && c.misc[1] == 0) {
-            // Fused combine: every unit of a 16-row tile (over all CTAs) bumps that tile's
-            // counter once this CTA's outputs are globally visible (one fence for all of them);
-            // the CTA that completes a tile's count runs the slot-ordered combine for it.
+        if (a.cmb_mode == 2) {
+            // this CTA's outputs must be globally visible before it counts them
+            if (lane == 0) c.misc[2] = c.misc[1] == 0;
             __threadfence();
             __syncwarp();
-            j = 0;
-            for (int u = u0; u < u1; ++u) {
-                int rt, g;
-                decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
-                int last = 0;
-                if (lane == 0) last = (atomicAdd(a.cmb_cnt + rt, 1) + 1 == c.goff[nt]);
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (!last) continue;
-                __threadfence();
-                const float* ev = static_cast<const float*>(a.out);
-                for (int o = lane; o < a.T * kRowTile; o += 32) {
-                    const int t = o / kRowTile, orow = rt * kRowTile + o % kRowTile;
-                    const size_t yo = static_cast<size_t>(t) * R + orow;
-                    float accv = a.seed ? __ldcg(a.seed + yo) : 0.0f;
-                    for (int q = 0; q < a.k; ++q) {
-                        const size_t r = static_cast<size_t>(t) * a.k + q;
-                        accv = __fadd_rn(accv, __fmul_rn(a.w[r], __ldcg(ev + r * R + orow)));
-                    }
-                    if (a.y_f32) a.y_f32[yo] = accv;
-                    static_cast<uint16_t*>(a.y)[yo] = float_to_adt_bits(accv, a.adt);
-                }
-                if (lane == 0) a.cmb_cnt[rt] = 0;
-            }
+            fused_combine();
         }
         return;
     }
@@ -498,26 +632,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     int it = 0, j = 0;
     int staged_j = -1, staged_g = -1;
     const uint16_t* in = a.in;
-    const bool copy_bits = kMmaBf16 || a.adt == 0;
-    // Phase 1 with at most tg tokens: every token's row is staged once here (x is per token and
-    // shared by every expert), and the units index it by token; otherwise rows are staged per
-    // group of routes when the group changes.
-    const bool tokmode = a.phase == 0 && a.T <= tg;
-    if (tokmode) {
-        if (warp < 8) {
-            const int t = warp;
-            float inv = 0.0f;
-            if (t < a.T) {
-                inv = stage_row<FMT>(in + static_cast<size_t>(t) * K, c.xs + static_cast<size_t>(t) * p.xstride,
-                                     c.xsum, t, K, nblk, prescale, copy_bits, lane);
-            } else if (FMT == FMT_INT4) {
-                for (int blk = lane; blk < nblk; blk += 32) c.xsum[blk * 8 + t] = 0.0f;
-            }
-            if (lane == 0) c.xinv[t] = inv;
-        }
-        named_bar(1, kNCW * 32);
-    }
-
     for (int u = u0; u < u1; ++u) {
         int rt, g;
         decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
@@ -639,13 +753,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                             ac[3] += d[3];
                         }
                     };
-                    // two blocks in flight per warp: independent fragments, interleavable
+                    // three blocks in flight per warp: independent fragments, interleavable
                     int i = warp;
-                    for (; i + kNCW < nbc; i += 2 * kNCW) {
+                    for (; i + 2 * kNCW < nbc; i += 3 * kNCW) {
                         block(i);
                         block(i + kNCW);
+                        block(i + 2 * kNCW);
                     }
-                    if (i < nbc) block(i);
+                    for (; i < nbc; i += kNCW) block(i);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&c.empty[s]);
@@ -677,6 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             if (lane == 0) mbar_arrive(&c.rfull[b]);
         }
     }
+    if (a.cmb_mode == 2) fused_combine();
 }
 
 }  // namespace
@@ -707,8 +823,7 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
         default: e = ensure_smem(gemv_kernel<FMT_INT4>, P.p.smem); break;
     }
     if (e != cudaSuccess) return e;
-    kern<<<num_sms, kThreads, P.p.smem, s>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms), dim3(kThreads), P.p.smem, s, P);
 }
 
 }  // namespace tsmoe

@@ -18,6 +18,8 @@ namespace {
 // y[t] = adt(seed[t] + sum_s w[t][s] * e[t*k+s]) with one rounded multiply and one rounded
 // add per slot, in slot order; the f32 sum is optionally returned.
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int t = blockIdx.y;
     const int j4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= a.T || j4 * 4 >= a.H) return;
@@ -87,8 +89,7 @@ __global__ void pack_kernel(int fmt, int nmat, int R, int K, const uint8_t* __re
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
     dim3 grid((a.H / 4 + 255) / 256, a.T);
-    combine_kernel<<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(256), 0, s, a);
 }
 
 cudaError_t launch_pack(int fmt, int nmat, int R, int K, const uint8_t* codes,

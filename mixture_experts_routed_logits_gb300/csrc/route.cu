@@ -84,6 +84,8 @@ router_kernel(RouteArgs a, int rb, int ns) {
     __shared__ __align__(8) uint64_t full[3];
     __shared__ __align__(8) uint64_t empty[3];
     __shared__ volatile int abort_flag;
+    pdl_wait();                 // x may come from the previous kernel
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     const int E = a.E, H = a.H, k = a.k;
@@ -242,6 +244,8 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
     __shared__ int cursor[kMaxExperts];
     __shared__ int wcnt[kBuildThreads / 32][kMaxExperts];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();                 // idx comes from the previous kernel
+    pdl_launch_dependents();
     for (int e = tid; e < E; e += kBuildThreads) cnt[e] = 0;
     __syncthreads();
     for (int r = tid; r < n; r += kBuildThreads) {
@@ -299,14 +303,13 @@ cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
         cudaError_t e = ensure_smem(router_kernel, p.smem);
         if (e != cudaSuccess) return e;
     }
-    router_kernel<<<a.T, kRouterWarps * 32, p.smem, s>>>(a, p.rb, p.ns);
-    return cudaGetLastError();
+    return launch_pdl(router_kernel, dim3(a.T), dim3(kRouterWarps * 32), p.smem, s, a, p.rb, p.ns);
 }
 
 cudaError_t launch_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off,
                                 int32_t* perm, int32_t* inv, int* status, cudaStream_t s) {
-    build_routes_kernel<<<1, kBuildThreads, 0, s>>>(idx, T * k, E, off, perm, inv, status);
-    return cudaGetLastError();
+    return launch_pdl(build_routes_kernel, dim3(1), dim3(kBuildThreads), 0, s, idx, T * k, E, off,
+                      perm, inv, status);
 }
 
 }  // namespace tsmoe
