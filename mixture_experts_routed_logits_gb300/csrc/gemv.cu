@@ -72,9 +72,9 @@ __host__ inline Plan make_plan(int fmt, int K, int tg_cap) {
                          + 2 * kMaxStages * 8                                // mbarriers
                          + (3 * kMaxExperts + 1 + 8) * 4                     // unit tables
                          + 2 * 8 * 4 + 4 * 8                                 // reducer hand-off
-                         + (kMaxExperts + 1 + kMaxLocalRoutes) * 4            // in-kernel routes
+                         + (kMaxExperts + 1 + 2 * kMaxLocalRoutes) * 4        // in-kernel routes
                          + 32 * 4                                            // combine tile list
-                         + 17 * 16;                                           // region padding
+                         + 18 * 16;                                           // region padding
     for (int ns = kMaxStages; ns >= 2; --ns) {
         const size_t ring = static_cast<size_t>(ns) * kStageBytes;
         if (ring + fixed >= static_cast<size_t>(kSmemBudget)) continue;
@@ -116,6 +116,7 @@ struct Carve {
     int* off_s;       // [257]: route offsets built in the kernel
     int* perm_s;      // [512]: route list built in the kernel
     int* ctile;       // [32]: row tiles this CTA combines in the current round
+    int* tok_s;       // [512]: token of each in-kernel route-list entry
 };
 
 __device__ inline Carve carve(unsigned char* base, const Plan& p, int K) {
@@ -144,6 +145,7 @@ __device__ inline Carve carve(unsigned char* base, const Plan& p, int K) {
     c.off_s = reinterpret_cast<int*>(take((kMaxExperts + 1) * 4));
     c.perm_s = reinterpret_cast<int*>(take(kMaxLocalRoutes * 4));
     c.ctile = reinterpret_cast<int*>(take(32 * 4));
+    c.tok_s = reinterpret_cast<int*>(take(kMaxLocalRoutes * 4));
     return c;
 }
 
@@ -157,6 +159,32 @@ __device__ __forceinline__ float act_fn(int act, float g, float u, float limit, 
     u = fminf(fmaxf(u, -limit), limit);
     return g / (1.0f + expf(-alpha * g)) * (u + 1.0f);
 }
+
+// Walks a CTA's units in order: unit u = RT * goff[j] + rt * ng + g (touched expert j, row
+// tile rt, group g of the ng = goff[j+1] - goff[j] groups of that expert).  Only the first unit
+// is decoded with a division; next() steps without any.
+struct UnitCursor {
+    int j, rt, g, ng;
+    __device__ __forceinline__ void seek(int u, int RT, const int* goff, int nt) {
+        j = 0;
+        while (j + 1 < nt && u >= RT * goff[j + 1]) ++j;
+        ng = goff[j + 1] - goff[j];
+        const int local = u - RT * goff[j];
+        rt = local / ng;
+        g = local - rt * ng;
+    }
+    // call only while a next unit exists (goff[j + 2] is read when the expert changes)
+    __device__ __forceinline__ void next(int RT, const int* goff) {
+        if (++g == ng) {
+            g = 0;
+            if (++rt == RT) {
+                rt = 0;
+                ++j;
+                ng = goff[j + 1] - goff[j];
+            }
+        }
+    }
+};
 
 // Unit u -> (touched index j, row tile, group).  `j` is a running hint (units are visited in
 // increasing order).
@@ -367,7 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 const int r = q * 32 + lane;
                 const bool valid = ev[q] >= 0 && ev[q] < a.E;
                 const unsigned peers = __match_any_sync(0xffffffffu, valid ? ev[q] : -1);
-                if (valid) c.perm_s[c.cnt[ev[q]] + __popc(peers & ((1u << lane) - 1u))] = r;
+                if (valid) {
+                    const int pos = c.cnt[ev[q]] + __popc(peers & ((1u << lane) - 1u));
+                    c.perm_s[pos] = r;
+                    c.tok_s[pos] = r / a.k;
+                }
                 __syncwarp();
                 if (valid && __ffs(peers) - 1 == lane) c.cnt[ev[q]] += __popc(peers);
                 __syncwarp();
@@ -512,24 +544,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         // tile, so the unit's biases are fetched one unit ahead (lane l < 16: bias 0 of row l,
         // lane 16 + l: bias 1) and handed out with shuffles.
         const int row = lane & 15;
-        int j = 0, jb = 0;
-        auto fetch_bias = [&](int u) {
-            int rt_, g_;
-            decode_unit(u, RT, c.goff, nt, jb, rt_, g_, c.cnt, tg);
+        UnitCursor cu, cb;              // the unit being reduced, the unit whose bias is fetched
+        cu.seek(u0, RT, c.goff, nt);
+        cb = cu;
+        auto fetch_bias = [&]() {
             const uint16_t* bp = lane < 16 ? a.b0 : (a.phase == 0 ? a.b1 : nullptr);
             if (!bp) return 0.0f;
             return __bfloat162float(__ushort_as_bfloat16(
-                bp[static_cast<size_t>(c.touched[jb]) * R + rt_ * kRowTile + row]));
+                bp[static_cast<size_t>(c.touched[cb.j]) * R + cb.rt * kRowTile + row]));
         };
-        float bias_next = fetch_bias(u0);
+        float bias_next = fetch_bias();
         for (int u = u0; u < u1; ++u) {
-            int rt, g;
-            decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
+            if (u > u0) cu.next(RT, c.goff);
+            const int j = cu.j, rt = cu.rt, g = cu.g;
             const int e = c.touched[j];
             const int cnt_g = min(tg, c.cnt[j] - g * tg);
             const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
             const float bias_cur = bias_next;
-            if (u + 1 < u1) bias_next = fetch_bias(u + 1);
+            if (u + 1 < u1) {
+                cb.next(RT, c.goff);
+                bias_next = fetch_bias();
+            }
             const float bias0 = __shfl_sync(0xffffffffu, bias_cur, row);
             const float bias1 = __shfl_sync(0xffffffffu, bias_cur, 16 + row);
             const int nl = u - u0, b = nl & 1;
@@ -576,16 +611,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
     if (warp == kNCW) {
         // ================================ producer warp =====================================
-        int it = 0, j = 0;
+        int it = 0, slot = 0;
+        uint32_t ph = 0;                // phase parity of the ring slot `slot`
+        UnitCursor cu;
+        cu.seek(u0, RT, c.goff, nt);
         for (int u = u0; u < u1; ++u) {
-            int rt, g;
-            decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
-            const int e = c.touched[j];
+            if (u > u0) cu.next(RT, c.goff);
+            const int rt = cu.rt;
+            const int e = c.touched[cu.j];
             for (int m = 0; m < nmat; ++m) {
                 const uint8_t* wbase = (m == 0 ? a.w0 : a.w1) + static_cast<size_t>(e) * a.mat_bytes;
                 for (int ch = 0; ch < nchunk; ++ch, ++it) {
-                    const int s = it % p.nstages;
-                    const uint32_t par = ((it / p.nstages) & 1) ^ 1;
+                    const int s = slot;
+                    const uint32_t par = ph ^ 1;
+                    if (++slot == p.nstages) {
+                        slot = 0;
+                        ph ^= 1;
+                    }
                     const int b0 = ch * p.nb;
                     const int nbc = min(p.nb, nblk - b0);
                     bool ok = true;
@@ -629,12 +671,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
     // ================================== consumer warps =========================================
     const int gid = lane >> 2, tid = lane & 3;
-    int it = 0, j = 0;
+    int it = 0, slot = 0;
+    uint32_t ph = 0;                    // phase parity of the ring slot `slot`
     int staged_j = -1, staged_g = -1;
     const uint16_t* in = a.in;
+    UnitCursor cu;
+    cu.seek(u0, RT, c.goff, nt);
     for (int u = u0; u < u1; ++u) {
-        int rt, g;
-        decode_unit(u, RT, c.goff, nt, j, rt, g, c.cnt, tg);
+        if (u > u0) cu.next(RT, c.goff);
+        const int j = cu.j, g = cu.g;
         const int e = c.touched[j];
         const int cnt_g = min(tg, c.cnt[j] - g * tg);
         const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
@@ -642,7 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         auto row_of = [&](int n) {
             if (!tokmode) return n < tg ? n : 0;
             if (n >= cnt_g) return 0;
-            return a.dense ? rbase + n : PERM[rbase + n] / a.k;
+            if (a.dense) return rbase + n;
+            return a.idx ? c.tok_s[rbase + n] : PERM[rbase + n] / a.k;
         };
         const int brow = row_of(gid);                 // activation row this lane feeds the mma
         const int xc0 = row_of(2 * tid), xc1 = row_of(2 * tid + 1);   // INT4 x-sum columns
@@ -686,8 +732,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
         for (int m = 0; m < nmat; ++m) {
             for (int ch = 0; ch < nchunk; ++ch, ++it) {
-                const int s = it % p.nstages;
-                const uint32_t par = (it / p.nstages) & 1;
+                const int s = slot;
+                const uint32_t par = ph;
+                if (++slot == p.nstages) {
+                    slot = 0;
+                    ph ^= 1;
+                }
                 const int b0 = ch * p.nb;
                 const int nbc = min(p.nb, nblk - b0);
                 bool ok = c.misc[1] == 0 && mbar_wait_bounded(&c.full[s], par);
