@@ -34,7 +34,8 @@ namespace tsmoe {
 namespace {
 
 constexpr int kNCW = 16;                      // consumer warps
-constexpr int kThreads = (kNCW + 2) * 32;     // + one producer warp + one reducer warp
+constexpr int kReducers = 2;                  // reducer warps: unit n goes to reducer n % 2
+constexpr int kThreads = (kNCW + 1 + kReducers) * 32;   // + one producer warp + the reducers
 constexpr int kMaxLocalRoutes = 512;          // route lists built inside the kernel up to this
 constexpr int kStageBytes = 24576;
 constexpr int kMaxStages = 6;
@@ -485,10 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // counters at once (one lane each) and lists the completed tiles, then all 17 warps
     // combine them.
     auto fused_combine = [&]() {
-        constexpr int kCmbThreads = (kNCW + 1) * 32;
+        constexpr int kCmbThreads = (kNCW + kReducers) * 32;
         named_bar(2, kCmbThreads);                  // combine decision published
         if (!c.misc[2]) return;
-        const int tix = warp < kNCW ? threadIdx.x : kNCW * 32 + lane;
+        const int tix = warp < kNCW ? threadIdx.x : threadIdx.x - 32;     // skip the producer warp
         const int per = a.T * kRowTile;
         const float* ev = static_cast<const float*>(a.out);
         int jl = 0;
@@ -535,34 +536,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
     };
 
-    if (warp == kNCW + 1) {
-        // ================================ reducer warp ======================================
-        // Sums the 16 compute warps' partials of each unit in fixed warp order, applies the
-        // prescale inverse, bias and activation, stores the unit's outputs; in phase 2 of a
-        // routed decode call the last unit of each 16-row tile also runs the slot-ordered
-        // combine for that tile.  Every output this lane touches has row (lane & 15) of the
-        // tile, so the unit's biases are fetched one unit ahead (lane l < 16: bias 0 of row l,
-        // lane 16 + l: bias 1) and handed out with shuffles.
+    if (warp > kNCW) {
+        // ================================ reducer warps =====================================
+        // Reducer r takes the units u0 + r, u0 + r + 2, ...: it sums the 16 compute warps'
+        // partials of a unit in fixed warp order, applies the prescale inverse, bias and
+        // activation and stores the unit's outputs.  Two of them, so that the reduction (a
+        // serial chain sharing its SM sub-partition with four compute warps) keeps pace.
+        // Every output this lane touches has row (lane & 15) of the tile, so the unit's biases
+        // are fetched one unit ahead (lane l < 16: bias 0 of row l, lane 16 + l: bias 1) and
+        // handed out with shuffles.
+        const int r = warp - kNCW - 1;
         const int row = lane & 15;
         UnitCursor cu, cb;              // the unit being reduced, the unit whose bias is fetched
-        cu.seek(u0, RT, c.goff, nt);
-        cb = cu;
+        auto step = [&](UnitCursor& x, int from) {     // x at unit `from` -> unit from + kReducers
+            for (int q = 1; q <= kReducers; ++q)
+                if (from + q < u1) x.next(RT, c.goff);
+        };
+        if (u0 + r < u1) {
+            cu.seek(u0 + r, RT, c.goff, nt);
+            cb = cu;
+        }
         auto fetch_bias = [&]() {
             const uint16_t* bp = lane < 16 ? a.b0 : (a.phase == 0 ? a.b1 : nullptr);
             if (!bp) return 0.0f;
             return __bfloat162float(__ushort_as_bfloat16(
                 bp[static_cast<size_t>(c.touched[cb.j]) * R + cb.rt * kRowTile + row]));
         };
-        float bias_next = fetch_bias();
-        for (int u = u0; u < u1; ++u) {
-            if (u > u0) cu.next(RT, c.goff);
+        float bias_next = u0 + r < u1 ? fetch_bias() : 0.0f;
+        for (int u = u0 + r; u < u1; u += kReducers) {
+            if (u > u0 + r) step(cu, u - kReducers);
             const int j = cu.j, rt = cu.rt, g = cu.g;
             const int e = c.touched[j];
             const int cnt_g = min(tg, c.cnt[j] - g * tg);
             const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
             const float bias_cur = bias_next;
-            if (u + 1 < u1) {
-                cb.next(RT, c.goff);
+            if (u + kReducers < u1) {
+                step(cb, u);
                 bias_next = fetch_bias();
             }
             const float bias0 = __shfl_sync(0xffffffffu, bias_cur, row);
@@ -601,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
         if (a.cmb_mode == 2) {
             // this CTA's outputs must be globally visible before it counts them
-            if (lane == 0) c.misc[2] = c.misc[1] == 0;
+            if (r == 0 && lane == 0) c.misc[2] = c.misc[1] == 0;
             __threadfence();
             __syncwarp();
             fused_combine();
