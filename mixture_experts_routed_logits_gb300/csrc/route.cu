@@ -13,13 +13,15 @@
 //     MiniMax "biased sigmoid scores with unbiased weights".
 // The pages run the top-k on the host after a blocking readback of the logits; here it stays
 // on the device, so the whole layer is one asynchronous stream of kernels.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace tsmoe {
 
 namespace {
 
-constexpr int kRouterWarps = 8;   // warps per token (experts are spread over them)
+constexpr int kRouterWarps = 8;   // warps per CTA
 
 
 // Order-preserving map of an f32 to u32 (larger float -> larger integer); -0 folds to +0 so
@@ -46,61 +48,116 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
 template <typename LoadB>
 __device__ __forceinline__ float warp_dot_fixed(const float* a, LoadB loadb, int H, int lane) {
     float p = 0.0f;
+#pragma unroll 8
     for (int j = lane; j < H; j += 32) p = __fmaf_rn(a[j], loadb(j), p);
     return warp_sum_xor(p);
 }
 
-// One CTA per token.  The router weights stream through shared memory in stages of `rb` rows
-// (one 1-D bulk copy per stage, up to `ns` stages in flight, mbarrier completion); warp w
-// computes the logit of row w of each stage.  The summation order of every logit is the fixed
-// one (lane l: fmaf over j, then the xor butterfly), so which warp computes it does not matter.
+// Router layout.  A CTA takes a tile of `tt` tokens and a group of `ec` experts; the `cl` expert
+// groups of a token tile form one thread-block cluster, so a decode batch of a few tokens still
+// spreads over many SMs.  The CTA's router rows stream through shared memory in stages of `rb`
+// rows (1-D bulk copies, `ns` stages in flight, mbarrier completion); each warp computes whole
+// logits (one row against every token of the tile, the tokens giving independent fma chains).
+// The summation order of every logit is the fixed one (lane l: fmaf over j, then the xor
+// butterfly), whichever warp or CTA computes it.  Rank 0 of the cluster then gathers each
+// token's E logits from the cluster's shared memory (distributed shared memory) and runs the
+// top-k, one warp per token.
+constexpr int kRouterTT = 8;      // tokens per CTA at most (one top-k warp each)
+
 struct RouterPlan {
-    int rb, ns;           // rows per stage, stages in flight
-    size_t smem;
+    int tt, cl, ec;       // tokens per CTA, CTAs per cluster, experts per CTA
+    int rb, ns;           // router rows per stage, stages in flight
+    int ntiles;           // token tiles
+    size_t xs_off, ring_off, lg_off, scr_off, smem;
 };
 
-__host__ inline RouterPlan router_plan(int H, int has_x) {
-    RouterPlan p{8, 3, 0};
-    if (!has_x) return p;
-    const size_t budget = 200 * 1024;
-    const size_t xs = static_cast<size_t>(H) * 4;
-    while (p.rb > 1 || p.ns > 1) {
-        const size_t need = xs + static_cast<size_t>(p.ns) * p.rb * H * 2 + 64;
-        if (need <= budget) break;
-        if (p.ns > 1) --p.ns; else p.rb /= 2;
+__host__ inline RouterPlan router_plan(int T, int H, int E, int has_x) {
+    RouterPlan p{};
+    const size_t budget = 210 * 1024;
+    if (has_x) {
+        p.tt = T <= 64 ? 1 : static_cast<int>(std::min<size_t>(kRouterTT, (96 * 1024) / (static_cast<size_t>(H) * 4)));
+        if (p.tt < 1) p.tt = 1;
+        p.ntiles = (T + p.tt - 1) / p.tt;
+        p.cl = 1;
+        while (p.cl < 8 && p.cl * 2 <= E && static_cast<long long>(p.ntiles) * p.cl < 128) p.cl *= 2;
+        p.ec = (E + p.cl - 1) / p.cl;
+    } else {
+        p.tt = kRouterTT;
+        p.ntiles = (T + p.tt - 1) / p.tt;
+        p.cl = 1;
+        p.ec = E;
     }
-    p.smem = xs + static_cast<size_t>(p.ns) * p.rb * H * 2 + 64;
+    p.xs_off = 0;
+    const size_t xs = has_x ? static_cast<size_t>(p.tt) * H * 4 : 0;
+    const size_t lg = static_cast<size_t>(p.tt) * p.ec * 4;
+    const size_t scr = static_cast<size_t>(kRouterWarps) * (2 * E + 2 * E) * 4;   // key, sg, ex, sel
+    const size_t fixed = ((xs + 127) & ~size_t(127)) + ((lg + 127) & ~size_t(127)) + scr + 256;
+    p.rb = std::min(p.ec, 32);
+    p.ns = 3;
+    while (has_x && p.rb > 1 && fixed + static_cast<size_t>(p.ns) * p.rb * H * 2 > budget) {
+        if (p.ns > 2) --p.ns; else p.rb = (p.rb + 1) / 2;
+    }
+    if (has_x && fixed + static_cast<size_t>(p.ns) * p.rb * H * 2 > budget) p.ns = 1;
+    p.ring_off = (xs + 127) & ~size_t(127);
+    const size_t ring = has_x ? static_cast<size_t>(p.ns) * p.rb * H * 2 : 0;
+    p.lg_off = p.ring_off + ((ring + 127) & ~size_t(127));
+    p.scr_off = p.lg_off + ((lg + 127) & ~size_t(127));
+    p.smem = p.scr_off + scr + 128;
     return p;
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t addr;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __global__ void __launch_bounds__(kRouterWarps * 32)
-router_kernel(RouteArgs a, int rb, int ns) {
+router_kernel(RouteArgs a, RouterPlan p) {
     extern __shared__ __align__(128) unsigned char rsm[];
-    __shared__ float key[kMaxExperts];
-    __shared__ float sg[kMaxExperts];
-    __shared__ float ex[kMaxExperts];
-    __shared__ int sel[kMaxExperts];
-    __shared__ float rnorm;
     __shared__ __align__(8) uint64_t full[3];
     __shared__ __align__(8) uint64_t empty[3];
+    __shared__ float rnorm[kRouterTT];
     __shared__ volatile int abort_flag;
     pdl_wait();                 // x may come from the previous kernel
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x;
     const int E = a.E, H = a.H, k = a.k;
-    if (t >= a.T) return;
+    const uint32_t rank = p.cl > 1 ? cluster_rank() : 0u;
+    const int tile = blockIdx.x / p.cl;
+    const int t0 = tile * p.tt;
+    const int ntok = max(0, min(p.tt, a.T - t0));
+    const int e0 = static_cast<int>(rank) * p.ec;
+    const int ne = max(0, min(p.ec, E - e0));
+    float* xs = reinterpret_cast<float*>(rsm + p.xs_off);          // [tt][H] f32
+    uint16_t* wst = reinterpret_cast<uint16_t*>(rsm + p.ring_off); // stages of rb rows
+    float* lg = reinterpret_cast<float*>(rsm + p.lg_off);          // [tt][ec] logits
+    if (threadIdx.x == 0) abort_flag = 0;
+    // the top-k warps fetch their router biases now, off the critical path
+    float bias_r[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        bias_r[i] = (a.bias && rank == 0 && warp < ntok && e < E) ? a.bias[e] : 0.0f;
+    }
 
-    // ---- step 1: optional RMSNorm + raw logits ------------------------------------------
+    // ---- step 1: optional RMSNorm + raw logits of this CTA's experts -----------------------
     if (a.x) {
-        float* xs = reinterpret_cast<float*>(rsm);
-        uint16_t* wst = reinterpret_cast<uint16_t*>(rsm + static_cast<size_t>(H) * 4);
-        const size_t stage_elems = static_cast<size_t>(rb) * H;
-        const int nst = (E + rb - 1) / rb;
-        const uint16_t* W = static_cast<const uint16_t*>(a.Wr);
+        const size_t stage_elems = static_cast<size_t>(p.rb) * H;
+        const int nst = (ne + p.rb - 1) / p.rb;
+        const uint16_t* W = static_cast<const uint16_t*>(a.Wr) + static_cast<size_t>(e0) * H;
         if (threadIdx.x == 0) {
-            abort_flag = 0;
-            for (int q = 0; q < ns; ++q) {
+            for (int q = 0; q < p.ns; ++q) {
                 mbar_init(&full[q], 1);
                 mbar_init(&empty[q], kRouterWarps);
             }
@@ -108,126 +165,186 @@ router_kernel(RouteArgs a, int rb, int ns) {
         }
         __syncthreads();
         auto issue = [&](int st) {
-            const int e0 = st * rb;
-            const int rows = min(rb, E - e0);
+            const int r0 = st * p.rb;
+            const int rows = min(p.rb, ne - r0);
             const uint32_t bytes = static_cast<uint32_t>(rows) * H * 2;
-            const int slot = st % ns;
+            const int slot = st % p.ns;
             mbar_arrive_expect_tx(&full[slot], bytes);
-            bulk_g2s(wst + slot * stage_elems, W + static_cast<size_t>(e0) * H, bytes, &full[slot]);
+            bulk_g2s(wst + slot * stage_elems, W + static_cast<size_t>(r0) * H, bytes, &full[slot]);
         };
         if (threadIdx.x == 0)
-            for (int st = 0; st < min(ns, nst); ++st) issue(st);
-        const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * H;
-        for (int j = threadIdx.x; j < H; j += blockDim.x) xs[j] = adt_bits_to_float(xr[j], a.adt);
+            for (int st = 0; st < min(p.ns, nst); ++st) issue(st);
+        // token rows -> f32 in shared memory (16-byte loads, all issued before use)
+        for (int q = 0; q < ntok; ++q) {
+            const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t0 + q) * H;
+            float* xq = xs + static_cast<size_t>(q) * H;
+            if ((H & 7) == 0 && (reinterpret_cast<uintptr_t>(xr) & 15) == 0) {
+                constexpr int kMaxV = 8;
+                const int nv = H / 8;
+                uint4 v[kMaxV];
+#pragma unroll
+                for (int i8 = 0; i8 < kMaxV; ++i8) {
+                    const int i = threadIdx.x + i8 * blockDim.x;
+                    if (i < nv) v[i8] = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+                }
+#pragma unroll
+                for (int i8 = 0; i8 < kMaxV; ++i8) {
+                    const int i = threadIdx.x + i8 * blockDim.x;
+                    if (i < nv) {
+                        const uint32_t w4[4] = {v[i8].x, v[i8].y, v[i8].z, v[i8].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            xq[8 * i + 2 * h] = adt_bits_to_float(static_cast<uint16_t>(w4[h] & 0xFFFF), a.adt);
+                            xq[8 * i + 2 * h + 1] = adt_bits_to_float(static_cast<uint16_t>(w4[h] >> 16), a.adt);
+                        }
+                    }
+                }
+                for (int j = kMaxV * blockDim.x * 8 + threadIdx.x; j < H; j += blockDim.x)
+                    xq[j] = adt_bits_to_float(xr[j], a.adt);
+            } else {
+                for (int j = threadIdx.x; j < H; j += blockDim.x) xq[j] = adt_bits_to_float(xr[j], a.adt);
+            }
+        }
         __syncthreads();
         if (a.rmsnorm) {
-            if (warp == 0) {
-                const float ss = warp_dot_fixed(xs, [&](int j) { return xs[j]; }, H, lane);
+            if (warp < ntok) {
+                const float* xq = xs + static_cast<size_t>(warp) * H;
+                const float ss = warp_dot_fixed(xq, [&](int j) { return xq[j]; }, H, lane);
                 const float ms = __fdiv_rn(ss, static_cast<float>(H));
-                if (lane == 0) rnorm = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+                if (lane == 0) rnorm[warp] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
             }
             __syncthreads();
-            const float r = rnorm;
-            uint16_t* xo = static_cast<uint16_t*>(a.xn_out) + static_cast<size_t>(t) * H;
-            for (int j = threadIdx.x; j < H; j += blockDim.x) {
-                const uint16_t b = float_to_adt_bits(__fmul_rn(xs[j], r), a.adt);
-                xo[j] = b;
-                xs[j] = adt_bits_to_float(b, a.adt);
+            for (int q = 0; q < ntok; ++q) {
+                const float r = rnorm[q];
+                float* xq = xs + static_cast<size_t>(q) * H;
+                uint16_t* xo = static_cast<uint16_t*>(a.xn_out) + static_cast<size_t>(t0 + q) * H;
+                for (int j = threadIdx.x; j < H; j += blockDim.x) {
+                    const uint16_t b = float_to_adt_bits(__fmul_rn(xq[j], r), a.adt);
+                    if (rank == 0) xo[j] = b;
+                    xq[j] = adt_bits_to_float(b, a.adt);
+                }
             }
             __syncthreads();
         }
         for (int st = 0; st < nst; ++st) {
-            const int slot = st % ns;
-            const bool ok = !abort_flag && mbar_wait_bounded(&full[slot], (st / ns) & 1);
+            const int slot = st % p.ns;
+            const int rows = min(p.rb, ne - st * p.rb);
+            const bool ok = !abort_flag && mbar_wait_bounded(&full[slot], (st / p.ns) & 1);
             if (!ok) {
                 if (lane == 0) abort_flag = 1;
-            } else if (warp < rb && st * rb + warp < E) {
-                const uint16_t* wr = wst + slot * stage_elems + static_cast<size_t>(warp) * H;
-                const float l = warp_dot_fixed(xs, [&](int j) { return adt_bits_to_float(wr[j], a.adt); },
-                                               H, lane);
-                if (lane == 0) key[st * rb + warp] = l;
+            } else {
+                for (int rr = warp; rr < rows; rr += kRouterWarps) {
+                    const uint16_t* wr = wst + slot * stage_elems + static_cast<size_t>(rr) * H;
+                    float acc[kRouterTT];
+#pragma unroll
+                    for (int q = 0; q < kRouterTT; ++q) acc[q] = 0.0f;
+#pragma unroll 4
+                    for (int j = lane; j < H; j += 32) {
+                        const float wv = adt_bits_to_float(wr[j], a.adt);
+#pragma unroll
+                        for (int q = 0; q < kRouterTT; ++q)
+                            if (q < ntok) acc[q] = __fmaf_rn(xs[static_cast<size_t>(q) * H + j], wv, acc[q]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < kRouterTT; ++q) {
+                        if (q >= ntok) break;
+                        const float l = warp_sum_xor(acc[q]);
+                        if (lane == 0) lg[q * p.ec + st * p.rb + rr] = l;
+                    }
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            if (threadIdx.x == 0 && st + ns < nst && !abort_flag) {
+            if (threadIdx.x == 0 && st + p.ns < nst && !abort_flag) {
                 // the slot is refilled once every warp has read it
-                if (mbar_wait_bounded(&empty[slot], (st / ns) & 1)) issue(st + ns);
+                if (mbar_wait_bounded(&empty[slot], (st / p.ns) & 1)) issue(st + p.ns);
                 else abort_flag = 1;
             }
         }
         // no copy may still be in flight when the CTA exits
         if (threadIdx.x == 0)
-            for (int st = max(0, nst - ns); st < nst; ++st)
-                mbar_wait_bounded(&full[st % ns], (st / ns) & 1);
+            for (int st = max(0, nst - p.ns); st < nst; ++st)
+                mbar_wait_bounded(&full[st % p.ns], (st / p.ns) & 1);
     } else {
-        const float* lr = a.logits_in + static_cast<size_t>(t) * E;
-        for (int e = threadIdx.x; e < E; e += blockDim.x) key[e] = lr[e];
+        for (int i = threadIdx.x; i < ntok * E; i += blockDim.x)
+            lg[i] = a.logits_in[static_cast<size_t>(t0) * E + i];
     }
     __syncthreads();
-    if (warp != 0) return;
+    if (p.cl > 1) cluster_sync_all();        // every CTA's logits are in its shared memory
 
-    // ---- step 2: keys per mode --------------------------------------------------------------
-    for (int e = lane; e < E; e += 32) {
-        const float l = key[e];
-        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
-        const float b = a.bias ? a.bias[e] : 0.0f;
-        float kv;
-        if (a.mode == MODE_SIGMOID_BIASED) {
-            const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-            sg[e] = s;
-            kv = a.bias ? __fadd_rn(s, b) : s;
-        } else {
-            kv = a.bias ? __fadd_rn(l, b) : l;
-        }
-        key[e] = kv;
-    }
-    __syncwarp();
-
-    // top-k by repeated warp arg-max; each lane owns experts lane + 32 i
-    uint64_t own[kMaxExperts / 32];
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = lane + 32 * i;
-        own[i] = e < E ? sel_key(key[e], e) : 0ull;
-    }
-    for (int s = 0; s < k; ++s) {
-        uint64_t best = 0ull;
-#pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) best = own[i] > best ? own[i] : best;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const uint64_t other = shfl_xor_u64(best, o);
-            best = other > best ? other : best;
-        }
-        const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
-        if ((e & 31) == lane) {
+    // ---- step 2: per token (one warp each, cluster rank 0): keys, top-k, weights --------------
+    if (rank == 0 && warp < ntok) {
+        const int t = t0 + warp;
+        float* key = reinterpret_cast<float*>(rsm + p.scr_off) + static_cast<size_t>(warp) * 4 * E;
+        float* sg = key + E;
+        float* ex = key + 2 * E;
+        int* sel = reinterpret_cast<int*>(key + 3 * E);
+        for (int e = lane; e < E; e += 32) {
+            const uint32_t owner = static_cast<uint32_t>(e / p.ec);
+            const float* src = lg + warp * p.ec + (e - static_cast<int>(owner) * p.ec);
+            const float l = p.cl > 1 ? ld_cluster_f32(src, owner) : *src;
+            if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
+            float b = 0.0f;
 #pragma unroll
             for (int i = 0; i < kMaxExperts / 32; ++i)
-                if (lane + 32 * i == e) own[i] = 0ull;
+                if (e == lane + 32 * i) b = bias_r[i];
+            float kv;
+            if (a.mode == MODE_SIGMOID_BIASED) {
+                const float sv = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
+                sg[e] = sv;
+                kv = a.bias ? __fadd_rn(sv, b) : sv;
+            } else {
+                kv = a.bias ? __fadd_rn(l, b) : l;
+            }
+            key[e] = kv;
         }
-        if (lane == 0) sel[s] = e;
+        __syncwarp();
+        // top-k by repeated warp arg-max; each lane owns experts lane + 32 i
+        uint64_t own[kMaxExperts / 32];
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+            const int e = lane + 32 * i;
+            own[i] = e < E ? sel_key(key[e], e) : 0ull;
+        }
+        for (int s = 0; s < k; ++s) {
+            uint64_t best = 0ull;
+#pragma unroll
+            for (int i = 0; i < kMaxExperts / 32; ++i) best = own[i] > best ? own[i] : best;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const uint64_t other = shfl_xor_u64(best, o);
+                best = other > best ? other : best;
+            }
+            const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+            if ((e & 31) == lane) {
+#pragma unroll
+                for (int i = 0; i < kMaxExperts / 32; ++i)
+                    if (lane + 32 * i == e) own[i] = 0ull;
+            }
+            if (lane == 0) sel[s] = e;
+        }
+        __syncwarp();
+        if (a.mode == MODE_SIGMOID_BIASED) {
+            for (int s = lane; s < k; s += 32) ex[s] = sg[sel[s]];
+        } else {
+            const float m = key[sel[0]];
+            for (int s = lane; s < k; s += 32) ex[s] = expf(__fsub_rn(key[sel[s]], m));
+        }
+        __syncwarp();
+        float sum = 0.0f;
+        if (lane == 0)
+            for (int s = 0; s < k; ++s) sum = __fadd_rn(sum, ex[s]);   // slot order
+        sum = __shfl_sync(0xffffffffu, sum, 0);
+        const bool aborted = a.x && abort_flag;
+        for (int s = lane; s < k; s += 32) {
+            float wv = __fdiv_rn(ex[s], sum);
+            if (a.mode == MODE_SOFTMAX_K_SCALED) wv = __fmul_rn(wv, a.scale[sel[s]]);
+            a.idx[static_cast<size_t>(t) * k + s] = aborted ? -1 : sel[s];   // -1: a wait gave up
+            a.w[static_cast<size_t>(t) * k + s] = wv;
+        }
     }
-    __syncwarp();
-
-    // ---- weights ------------------------------------------------------------------------------
-    if (a.mode == MODE_SIGMOID_BIASED) {
-        for (int s = lane; s < k; s += 32) ex[s] = sg[sel[s]];
-    } else {
-        const float m = key[sel[0]];
-        for (int s = lane; s < k; s += 32) ex[s] = expf(__fsub_rn(key[sel[s]], m));
-    }
-    __syncwarp();
-    float sum = 0.0f;
-    if (lane == 0)
-        for (int s = 0; s < k; ++s) sum = __fadd_rn(sum, ex[s]);   // slot order
-    sum = __shfl_sync(0xffffffffu, sum, 0);
-    const bool aborted = a.x && abort_flag;
-    for (int s = lane; s < k; s += 32) {
-        float wv = __fdiv_rn(ex[s], sum);
-        if (a.mode == MODE_SOFTMAX_K_SCALED) wv = __fmul_rn(wv, a.scale[sel[s]]);
-        a.idx[static_cast<size_t>(t) * k + s] = aborted ? -1 : sel[s];   // -1: the wait gave up
-        a.w[static_cast<size_t>(t) * k + s] = wv;
-    }
+    // the other CTAs of the cluster keep their shared memory until rank 0 has read it
+    if (p.cl > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -298,12 +415,24 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
 
 cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
-    const RouterPlan p = router_plan(a.H, a.x != nullptr);
-    if (p.smem > 40 * 1024) {
-        cudaError_t e = ensure_smem(router_kernel, p.smem);
-        if (e != cudaSuccess) return e;
-    }
-    return launch_pdl(router_kernel, dim3(a.T), dim3(kRouterWarps * 32), p.smem, s, a, p.rb, p.ns);
+    const RouterPlan p = router_plan(a.T, a.H, a.E, a.x != nullptr);
+    cudaError_t e = ensure_smem(router_kernel, p.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ntiles * p.cl);
+    cfg.blockDim = dim3(kRouterWarps * 32);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = static_cast<unsigned>(p.cl);
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, router_kernel, a, p);
 }
 
 cudaError_t launch_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off,
