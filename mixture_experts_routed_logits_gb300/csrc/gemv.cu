@@ -27,7 +27,7 @@
 //     [2^14, 2^15)), exact for bf16 inputs in f16's range, undone in f32 after the sum.
 //   * Partial sums of the eight warps are reduced through shared memory in fixed warp order:
 //     results are deterministic run to run.
-#include "common.cuh"
+#include "gemv_common.cuh"
 
 namespace tsmoe {
 
@@ -36,7 +36,7 @@ namespace {
 constexpr int kNCW = 16;                      // consumer warps
 constexpr int kReducers = 2;                  // reducer warps: unit n goes to reducer n % 2
 constexpr int kThreads = (kNCW + 1 + kReducers) * 32;   // + one producer warp + the reducers
-constexpr int kMaxLocalRoutes = 512;          // route lists built inside the kernel up to this
+
 constexpr int kStageBytes = 24576;
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 225 * 1024;
@@ -150,17 +150,6 @@ __device__ inline Carve carve(unsigned char* base, const Plan& p, int K) {
     return c;
 }
 
-__device__ __forceinline__ float act_fn(int act, float g, float u, float limit, float alpha) {
-    if (act == ACT_SILU) return g / (1.0f + expf(-g)) * u;
-    if (act == ACT_GELU) {
-        const float c = 0.7978845608028654f;   // sqrt(2/pi)
-        return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g))) * u;
-    }
-    g = fminf(g, limit);
-    u = fminf(fmaxf(u, -limit), limit);
-    return g / (1.0f + expf(-alpha * g)) * (u + 1.0f);
-}
-
 // Walks a CTA's units in order: unit u = RT * goff[j] + rt * ng + g (touched expert j, row
 // tile rt, group g of the ng = goff[j+1] - goff[j] groups of that expert).  Only the first unit
 // is decoded with a division; next() steps without any.
@@ -198,113 +187,6 @@ __device__ __forceinline__ void decode_unit(int u, int RT, const int* goff, int 
     g = local % ng;
 }
 
-// Stages one activation row into shared memory in the mma operand type: f16 with a
-// power-of-two prescale (max |x| * 2^ks in [2^14, 2^15)) when bf16 activations feed the f16
-// mma, else the bits as they are; element order inside each 8-group is natural, or
-// (0,4,1,5,2,6,3,7) for INT4.  For K <= 3072 the row is read once, with every load issued
-// before any is used; returns the inverse prescale.
-template <int FMT>
-__device__ __forceinline__ float stage_row(const uint16_t* __restrict__ src, unsigned char* xrow,
-                                           float* xsum, int col, int K, int nblk, bool prescale,
-                                           bool copy_bits, int lane) {
-    auto store_block = [&](int blk, const uint32_t (&wv)[16], float scl) {
-        uint16_t o[32];
-        float bsum = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const uint16_t bits = static_cast<uint16_t>((q & 1) ? (wv[q >> 1] >> 16) : (wv[q >> 1] & 0xFFFF));
-            uint16_t ob;
-            if (copy_bits) {
-                ob = bits;
-            } else {
-                const float v = __fmul_rn(__bfloat162float(__ushort_as_bfloat16(bits)), scl);
-                ob = __half_as_ushort(__float2half_rn(v));
-            }
-            if (FMT == FMT_INT4) bsum += __half2float(__ushort_as_half(ob));
-            o[q] = ob;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-#pragma unroll
-            for (int pr = 0; pr < 4; ++pr) {
-                uint16_t lo, hi;
-                if (FMT == FMT_INT4) { lo = o[q8 * 8 + pr]; hi = o[q8 * 8 + pr + 4]; }
-                else { lo = o[q8 * 8 + 2 * pr]; hi = o[q8 * 8 + 2 * pr + 1]; }
-                pk[q8 * 4 + pr] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-            }
-        }
-        uint4* d4 = reinterpret_cast<uint4*>(xrow + static_cast<size_t>(blk) * 64);
-#pragma unroll
-        for (int h = 0; h < 4; ++h) d4[h] = make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
-        if (FMT == FMT_INT4) xsum[blk * 8 + col] = bsum;
-    };
-    auto absmax16 = [&](const uint32_t (&wv)[16]) {
-        float mx = 0.0f;
-#pragma unroll
-        for (int h = 0; h < 16; ++h) {
-            mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(wv[h] & 0xFFFF))));
-            mx = fmaxf(mx, fabsf(__bfloat162float(__ushort_as_bfloat16(wv[h] >> 16))));
-        }
-        return mx;
-    };
-    auto prescale_of = [&](float mx, float& scl, float& inv) {
-        scl = inv = 1.0f;
-        if (mx > 0.0f && mx < 3.0e38f) {
-            int ex;
-            frexpf(mx, &ex);            // mx = f * 2^ex, f in [0.5, 1)
-            const int ks = max(-120, min(120, 15 - ex));
-            scl = __uint_as_float(static_cast<uint32_t>(ks + 127) << 23);
-            inv = __uint_as_float(static_cast<uint32_t>(127 - ks) << 23);
-        }
-    };
-    float scl = 1.0f, inv = 1.0f;
-    if (nblk <= 96) {
-        uint32_t wv[3][16];
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-            const int blk = lane + 32 * q;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (blk < nblk) v = __ldg(reinterpret_cast<const uint4*>(src + blk * kBlockK) + h);
-                wv[q][4 * h] = v.x; wv[q][4 * h + 1] = v.y; wv[q][4 * h + 2] = v.z; wv[q][4 * h + 3] = v.w;
-            }
-        }
-        if (prescale) {
-            float mx = fmaxf(fmaxf(absmax16(wv[0]), absmax16(wv[1])), absmax16(wv[2]));
-            prescale_of(warp_max(mx), scl, inv);
-        }
-#pragma unroll
-        for (int q = 0; q < 3; ++q)
-            if (lane + 32 * q < nblk) store_block(lane + 32 * q, wv[q], scl);
-        return inv;
-    }
-    if (prescale) {
-        float mx = 0.0f;
-        for (int blk = lane; blk < nblk; blk += 32) {
-            uint32_t wv[16];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + blk * kBlockK) + h);
-                wv[4 * h] = v.x; wv[4 * h + 1] = v.y; wv[4 * h + 2] = v.z; wv[4 * h + 3] = v.w;
-            }
-            mx = fmaxf(mx, absmax16(wv));
-        }
-        prescale_of(warp_max(mx), scl, inv);
-    }
-    for (int blk = lane; blk < nblk; blk += 32) {
-        uint32_t wv[16];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + blk * kBlockK) + h);
-            wv[4 * h] = v.x; wv[4 * h + 1] = v.y; wv[4 * h + 2] = v.z; wv[4 * h + 3] = v.w;
-        }
-        store_block(blk, wv, scl);
-    }
-    return inv;
-}
-
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ KParams P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -340,111 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const bool copy_bits = kMmaBf16 || a.adt == 0;
     if (warp == kNCW + 1) {
         // ---- route list (decode sizes) and unit tables, built by one warp --------------------
-        if (a.idx) {
-            // counting sort of the route ids by expert, ascending id inside an expert: chunks of
-            // 32 routes, experts of a chunk grouped with match_any, one counter update per group
-            const int n = a.T * a.k;
-            int ev[kMaxLocalRoutes / 32];
-#pragma unroll
-            for (int q = 0; q < kMaxLocalRoutes / 32; ++q) {
-                const int r = q * 32 + lane;
-                ev[q] = r < n ? a.idx[r] : -1;
-            }
-            for (int e = lane; e <= a.E; e += 32) c.off_s[e] = 0;
-            __syncwarp();
-#pragma unroll
-            for (int q = 0; q < kMaxLocalRoutes / 32; ++q) {
-                if (q * 32 >= n) break;
-                const int r = q * 32 + lane;
-                const bool valid = ev[q] >= 0 && ev[q] < a.E;
-                if (r < n && !valid) report_error(a.status, DEV_ERR_INVALID);
-                const unsigned peers = __match_any_sync(0xffffffffu, valid ? ev[q] : -1);
-                if (valid && __ffs(peers) - 1 == lane) c.off_s[ev[q] + 1] += __popc(peers);
-                __syncwarp();
-            }
-            // inclusive scan of the counts (off_s[1..E]) -> route offsets; lane l owns 8 entries
-            {
-                int loc[8], sum = 0;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int e = lane * 8 + q;
-                    loc[q] = e < a.E ? c.off_s[e + 1] : 0;
-                    sum += loc[q];
-                }
-                int incl = sum;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d) incl += v;
-                }
-                int run = incl - sum;
-                __syncwarp();
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int e = lane * 8 + q;
-                    run += loc[q];
-                    if (e < a.E) {
-                        c.off_s[e + 1] = run;
-                        c.cnt[e] = run - loc[q];          // placement cursor (cnt reused)
-                    }
-                }
-                __syncwarp();
-            }
-#pragma unroll
-            for (int q = 0; q < kMaxLocalRoutes / 32; ++q) {
-                if (q * 32 >= n) break;
-                const int r = q * 32 + lane;
-                const bool valid = ev[q] >= 0 && ev[q] < a.E;
-                const unsigned peers = __match_any_sync(0xffffffffu, valid ? ev[q] : -1);
-                if (valid) {
-                    const int pos = c.cnt[ev[q]] + __popc(peers & ((1u << lane) - 1u));
-                    c.perm_s[pos] = r;
-                    c.tok_s[pos] = r / a.k;
-                }
-                __syncwarp();
-                if (valid && __ffs(peers) - 1 == lane) c.cnt[ev[q]] += __popc(peers);
-                __syncwarp();
-            }
-        }
-        // touched experts in ascending order with their route counts and group prefix
-        int nt = 0, acc = 0;
-        if (a.dense) {
-            if (lane == 0) {
-                c.touched[0] = 0;
-                c.cnt[0] = a.T;
-                c.goff[0] = 0;
-            }
-            acc = (a.T + tg - 1) / tg;
-            nt = 1;
-        } else {
-            for (int e0 = 0; e0 < a.E; e0 += 32) {
-                const int e = e0 + lane;
-                const int n = e < a.E ? OFF[e + 1] - OFF[e] : 0;
-                const unsigned m = __ballot_sync(0xffffffffu, n > 0);
-                const int groups = n > 0 ? (n + tg - 1) / tg : 0;
-                int incl = groups;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d) incl += v;
-                }
-                __syncwarp();
-                if (n > 0) {
-                    const int pos = nt + __popc(m & ((1u << lane) - 1u));
-                    c.touched[pos] = e;
-                    c.cnt[pos] = n;
-                    c.goff[pos] = acc + incl - groups;
-                }
-                __syncwarp();
-                acc += __shfl_sync(0xffffffffu, incl, 31);
-                nt += __popc(m);
-            }
-        }
-        if (lane == 0) {
-            c.goff[nt] = acc;
-            c.misc[0] = nt;
-            c.misc[1] = 0;
-        }
+        build_route_tables(a, tg, lane, c.off_s, c.perm_s, c.tok_s, c.touched, c.cnt, c.goff, c.misc);
     } else if (warp == kNCW) {
         if (lane == 0) {
             for (int s = 0; s < p.nstages; ++s) {
@@ -861,6 +639,9 @@ int gemv_pick_tg(int K) { return make_plan(FMT_F16, K, 8).tg; }
 size_t gemv_smem_bytes(int fmt, int K, int tg) { return make_plan(fmt, K, tg).smem; }
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
+    // INT4 weights: the warp-independent kernel of gemv_sk.cu (measured faster there; for MXFP4
+    // at the gpt-oss shapes this kernel with its two reducer warps is still ahead)
+    if (a.fmt == FMT_INT4 && gemv_sk_fits(a.fmt, a.K, a.T)) return launch_gemv_sk(a, num_sms, s);
     KParams P;
     P.a = a;
     const int tmax = a.dense ? a.T : a.T;   // tokens per expert never exceed T
