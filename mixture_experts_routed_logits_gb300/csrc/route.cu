@@ -71,19 +71,16 @@ struct RouterPlan {
     size_t xs_off, ring_off, lg_off, scr_off, smem;
 };
 
-__host__ inline RouterPlan router_plan(int T, int H, int E, int has_x) {
+__host__ inline RouterPlan router_plan_tt(int T, int H, int E, int has_x, int tt) {
     RouterPlan p{};
     const size_t budget = 210 * 1024;
+    p.tt = tt;
+    p.ntiles = (T + p.tt - 1) / p.tt;
     if (has_x) {
-        p.tt = T <= 64 ? 1 : static_cast<int>(std::min<size_t>(kRouterTT, (96 * 1024) / (static_cast<size_t>(H) * 4)));
-        if (p.tt < 1) p.tt = 1;
-        p.ntiles = (T + p.tt - 1) / p.tt;
         p.cl = 1;
         while (p.cl < 8 && p.cl * 2 <= E && static_cast<long long>(p.ntiles) * p.cl < 128) p.cl *= 2;
         p.ec = (E + p.cl - 1) / p.cl;
     } else {
-        p.tt = kRouterTT;
-        p.ntiles = (T + p.tt - 1) / p.tt;
         p.cl = 1;
         p.ec = E;
     }
@@ -103,6 +100,17 @@ __host__ inline RouterPlan router_plan(int T, int H, int E, int has_x) {
     p.lg_off = p.ring_off + ((ring + 127) & ~size_t(127));
     p.scr_off = p.lg_off + ((lg + 127) & ~size_t(127));
     p.smem = p.scr_off + scr + 128;
+    return p;
+}
+
+// Tokens per CTA: 1 for decode batches; for prefill as many as fit (f32 rows within 96 KB) while a
+// stage still holds a router row for every warp.
+__host__ inline RouterPlan router_plan(int T, int H, int E, int has_x) {
+    if (!has_x) return router_plan_tt(T, H, E, 0, kRouterTT);
+    int tt = T <= 64 ? 1 : static_cast<int>(std::min<size_t>(kRouterTT, (96 * 1024) / (static_cast<size_t>(H) * 4)));
+    if (tt < 1) tt = 1;
+    RouterPlan p = router_plan_tt(T, H, E, 1, tt);
+    while (p.tt > 1 && p.rb < std::min(p.ec, kRouterWarps)) p = router_plan_tt(T, H, E, 1, p.tt - 1);
     return p;
 }
 
