@@ -123,6 +123,17 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
         L.hinv = take(Tk * 4);
         L.h16 = take(Tk * ex->I * 2);
     }
+    // split-K partials of the tensor-core path for decode-sized calls (few routes, so the few
+    // (expert, row block) tiles are cut along K to reach every SM): [part][route][2][rows] f32
+    // and one counter per (tile group, 32-row slice) and phase
+    if (Tk > 0 && Tk <= 64) {
+        const size_t rmax = ex->I > ex->H ? ex->I : ex->H;
+        const size_t e_eff = static_cast<size_t>(ex->E) < Tk ? static_cast<size_t>(ex->E) : Tk;
+        L.max_split = kMaxSplit;
+        L.part = take(static_cast<size_t>(kMaxSplit) * Tk * 2 * rmax * 4);
+        L.tcnt_n = ((rmax + 127) / 128) * (Tk / 16 + e_eff) * 4;
+        L.tcnt = take(2 * L.tcnt_n * 4);
+    }
     L.total = a;
     return L;
 }
