@@ -89,7 +89,7 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
 }
 
 struct WsLayout {
-    size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hmax, hinv, h16, cmb, part, tcnt, total;
+    size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hinv, h16, cmb, part, tcnt, total;
     size_t tcnt_n;        // split-K group counters per phase
     int max_split;        // > 1 when the partials fit (decode sizes)
 };
@@ -119,7 +119,6 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
     L.cmb = take(static_cast<size_t>(ex->H / kRowTile) * 4);   // fused-combine counters
     if (ex->fmt == FMT_MXFP4) {      // f16 operands of the MXFP4 tensor-core path
         L.xinv = take(Tk * 4);
-        L.hmax = take(Tk * 4);
         L.hinv = take(Tk * 4);
         L.h16 = take(Tk * ex->I * 2);
     }
@@ -337,10 +336,10 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         const int Tk = T * k;
         uint16_t* xs = reinterpret_cast<uint16_t*>(W + L.xs);
         float* xinv = quant_gemm ? reinterpret_cast<float*>(W + L.xinv) : nullptr;
-        unsigned* hmax = quant_gemm ? reinterpret_cast<unsigned*>(W + L.hmax) : nullptr;
+
         if (quant_gemm)
             e = launch_gather_rows_f16(static_cast<const uint16_t*>(x), adt, perm, k, ex->H, Tk, xs,
-                                       xinv, hmax, st);
+                                       xinv, st);
         else
             e = launch_gather_rows(static_cast<const uint16_t*>(x), perm, k, ex->H, Tk, xs, st);
         if (e == cudaSuccess) e = phase_mark(0, st);
@@ -368,7 +367,6 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         G.perm = perm;
         G.status = status;
         G.col_scale = xinv;
-        G.hmax = hmax;
         G.max_split = L.max_split;
         G.part = L.max_split > 1 ? reinterpret_cast<float*>(W + L.part) : nullptr;
         G.cnt = L.max_split > 1 ? reinterpret_cast<int*>(W + L.tcnt) : nullptr;
@@ -386,13 +384,11 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         G.K = ex->I;
         G.act_in = W + L.h;
         G.out = W + L.e;
-        G.hmax = nullptr;
         if (L.max_split > 1) G.cnt = reinterpret_cast<int*>(W + L.tcnt) + L.tcnt_n;
         if (quant_gemm) {
             uint16_t* h16 = reinterpret_cast<uint16_t*>(W + L.h16);
             float* hinv = reinterpret_cast<float*>(W + L.hinv);
-            e = launch_h_to_f16(reinterpret_cast<const uint16_t*>(W + L.h), adt, hmax, ex->I, Tk, h16,
-                                hinv, st);
+            e = launch_h_to_f16(reinterpret_cast<const uint16_t*>(W + L.h), adt, ex->I, Tk, h16, hinv, st);
             if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: h to f16");
             G.act_in = h16;
             G.col_scale = hinv;

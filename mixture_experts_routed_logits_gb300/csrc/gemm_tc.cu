@@ -468,11 +468,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     float d0[16], d1[16];
                     tmem_ld16_pair(tq + c0, tq + 256 + c0, d0, d1);
                     if (a.phase == 0) {
-                        unsigned hm[16];
 #pragma unroll
                         for (int t = 0; t < 16; ++t) {
                             const int c = c0 + t;
-                            hm[t] = 0u;
                             if (va && c < n_valid) {
                                 float gv = d0[t], uv = d1[t];
                                 if (QUANT) {
@@ -483,16 +481,6 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                                 const float h = act_fn(a.act, gv + bg, uv + bu, a.limit, a.alpha);
                                 const uint16_t hb = float_to_adt_bits(h, a.adt);
                                 hout[static_cast<size_t>(p0 + c) * R + ra] = hb;
-                                if (QUANT) hm[t] = __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt)));
-                            }
-                        }
-                        if (QUANT) {
-                            // per-route max |h| (positive floats order like their bit patterns):
-                            // reduced over the warp's 32 rows first, one atomic per warp and column
-#pragma unroll
-                            for (int t = 0; t < 16; ++t) {
-                                const unsigned mv = __reduce_max_sync(0xffffffffu, hm[t]);
-                                if (lane == 0 && c0 + t < n_valid) atomicMax(a.hmax + p0 + c0 + t, mv);
                             }
                         }
                     } else {
@@ -555,16 +543,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 }
                 const float inv = QUANT ? a.col_scale[p0 + c] : 1.0f;
                 if (a.phase == 0) {
-                    unsigned hm = 0u;
                     if (va) {
                         const float h = act_fn(a.act, x0 * inv + bg, x1 * inv + bu, a.limit, a.alpha);
-                        const uint16_t hb = float_to_adt_bits(h, a.adt);
-                        hout[static_cast<size_t>(p0 + c) * R + ra] = hb;
-                        hm = __float_as_uint(fabsf(adt_bits_to_float(hb, a.adt)));
-                    }
-                    if (QUANT) {
-                        const unsigned mv = __reduce_max_sync(0xffffffffu, hm);
-                        if (lane == 0) atomicMax(a.hmax + p0 + c, mv);
+                        hout[static_cast<size_t>(p0 + c) * R + ra] = float_to_adt_bits(h, a.adt);
                     }
                 } else {
                     const size_t r = static_cast<size_t>(a.perm[p0 + c]);
@@ -618,12 +599,11 @@ __device__ __forceinline__ float block_max128(float v, float* red) {
 }
 
 // Route-ordered activations for the f16 tensor-core operand: xs[p] = f16(x[perm[p]/k] * 2^ks),
-// inv[p] = 2^-ks; also clears hmax[p] for the phase-1 epilogue.
+// inv[p] = 2^-ks.
 __global__ void __launch_bounds__(128) gather_rows_f16_kernel(const uint16_t* __restrict__ x, int adt,
                                                               const int32_t* __restrict__ perm, int k,
                                                               int H, int n, uint16_t* __restrict__ xs,
-                                                              float* __restrict__ inv_out,
-                                                              unsigned* __restrict__ hmax) {
+                                                              float* __restrict__ inv_out) {
     __shared__ float red[4];
     pdl_wait();
     pdl_launch_dependents();
@@ -638,24 +618,24 @@ __global__ void __launch_bounds__(128) gather_rows_f16_kernel(const uint16_t* __
     uint16_t* dst = xs + static_cast<size_t>(p) * H;
     for (int i = threadIdx.x; i < H; i += blockDim.x)
         dst[i] = __half_as_ushort(__float2half_rn(__fmul_rn(adt_bits_to_float(src[i], adt), scl)));
-    if (threadIdx.x == 0) {
-        inv_out[p] = inv;
-        hmax[p] = 0u;
-    }
+    if (threadIdx.x == 0) inv_out[p] = inv;
 }
 
-// h (16-bit, route order) -> f16 with a per-route prescale from hmax[p].
-__global__ void __launch_bounds__(128) h_to_f16_kernel(const uint16_t* __restrict__ h, int adt,
-                                                       const unsigned* __restrict__ hmax, int I, int n,
-                                                       uint16_t* __restrict__ h16,
+// h (16-bit, route order) -> f16 with a per-route power-of-two prescale from max |h| of the row.
+__global__ void __launch_bounds__(128) h_to_f16_kernel(const uint16_t* __restrict__ h, int adt, int I,
+                                                       int n, uint16_t* __restrict__ h16,
                                                        float* __restrict__ inv_out) {
+    __shared__ float red[4];
     pdl_wait();
     pdl_launch_dependents();
     const int p = blockIdx.x;
     if (p >= n) return;
-    float scl, inv;
-    prescale_of(__uint_as_float(hmax[p]), scl, inv);
     const uint16_t* src = h + static_cast<size_t>(p) * I;
+    float mx = 0.0f;
+    for (int i = threadIdx.x; i < I; i += blockDim.x) mx = fmaxf(mx, fabsf(adt_bits_to_float(src[i], adt)));
+    mx = block_max128(mx, red);
+    float scl, inv;
+    prescale_of(mx, scl, inv);
     uint16_t* dst = h16 + static_cast<size_t>(p) * I;
     for (int i = threadIdx.x; i < I; i += blockDim.x)
         dst[i] = __half_as_ushort(__float2half_rn(__fmul_rn(adt_bits_to_float(src[i], adt), scl)));
@@ -727,15 +707,15 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, in
 }
 
 cudaError_t launch_gather_rows_f16(const uint16_t* x, int adt, const int32_t* perm, int k, int H,
-                                   int n, uint16_t* xs, float* inv, unsigned* hmax, cudaStream_t s) {
+                                   int n, uint16_t* xs, float* inv, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    return launch_pdl(gather_rows_f16_kernel, dim3(n), dim3(128), 0, s, x, adt, perm, k, H, n, xs, inv, hmax);
+    return launch_pdl(gather_rows_f16_kernel, dim3(n), dim3(128), 0, s, x, adt, perm, k, H, n, xs, inv);
 }
 
-cudaError_t launch_h_to_f16(const uint16_t* h, int adt, const unsigned* hmax, int I, int n,
-                            uint16_t* h16, float* inv, cudaStream_t s) {
+cudaError_t launch_h_to_f16(const uint16_t* h, int adt, int I, int n, uint16_t* h16, float* inv,
+                            cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    return launch_pdl(h_to_f16_kernel, dim3(n), dim3(128), 0, s, h, adt, hmax, I, n, h16, inv);
+    return launch_pdl(h_to_f16_kernel, dim3(n), dim3(128), 0, s, h, adt, I, n, h16, inv);
 }
 
 // Launch shape: routes per tile, ring depth and K split.  Decode-sized calls (few routes) use

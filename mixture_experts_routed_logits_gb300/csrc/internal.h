@@ -116,7 +116,6 @@ struct GemmArgs {
     int quant;                    // 1: w0/w1 are packed MXFP4 (dequantised to f16 in smem)
     size_t mat_bytes;             // packed bytes per expert matrix (quant)
     const float* col_scale;       // quant: per route-list position, undoes the f16 prescale
-    unsigned* hmax;               // quant phase 0: per position max |h| (f32 bits, atomicMax)
     int max_split;                // > 1: K may be split in up to this many parts (needs part/cnt)
     float* part;                  // split-K partials [max_split][rows_in][2][R] f32
     int* cnt;                     // split-K group counters (zero before the launch)
@@ -125,8 +124,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
                                uint16_t* xs, cudaStream_t s);
 cudaError_t launch_gather_rows_f16(const uint16_t* x, int adt, const int32_t* perm, int k, int H,
-                                   int n, uint16_t* xs, float* inv, unsigned* hmax, cudaStream_t s);
-cudaError_t launch_h_to_f16(const uint16_t* h, int adt, const unsigned* hmax, int I, int n,
+                                   int n, uint16_t* xs, float* inv, cudaStream_t s);
+cudaError_t launch_h_to_f16(const uint16_t* h, int adt, int I, int n,
                             uint16_t* h16, float* inv, cudaStream_t s);
 
 // records the thread's ts_last_error() message (defined in api.cu); returns `status`
