@@ -725,7 +725,9 @@ static TcLayout tc_layout(const GemmArgs& a, int num_sms, size_t* smem) {
     TcLayout L{};
     const int Tk = a.rows_in;
     L.bn = Tk <= 256 ? 64 : 256;
-    const size_t tail = 4096 + 1024;
+    // shared-memory tail (barriers and the item tables) plus 1 KB for aligning the base to 1024
+    constexpr size_t kTailBytes = (sizeof(SmemTail) + 255) / 256 * 256;
+    const size_t tail = kTailBytes + 1024;
     const size_t budget = 227 * 1024;
     const int bbytes = (L.bn / 64) * kBBox;
     if (a.quant) {
@@ -749,7 +751,7 @@ static TcLayout tc_layout(const GemmArgs& a, int num_sms, size_t* smem) {
         if (S > nkb / 4) S = nkb / 4;
         L.S = S < 1 ? 1 : S;
     }
-    *smem = 1024 + L.a_ring_bytes + static_cast<size_t>(L.nslot) * L.slot_bytes + 4096;
+    *smem = 1024 + L.a_ring_bytes + static_cast<size_t>(L.nslot) * L.slot_bytes + kTailBytes;
     return L;
 }
 
