@@ -195,7 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int K = a.K, R = a.R;
     const int nblk = K / kBlockK;
     const int RT = R / kRowTile;
-    const int nmat = a.phase == 0 ? 2 : 1;
     const int nchunk = (nblk + p.nb - 1) / p.nb;
     const int tg = p.tg;
     constexpr bool kPacked = (FMT == FMT_MXFP4 || FMT == FMT_INT4);
@@ -252,23 +251,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         for (int i = threadIdx.x; i < a.cmb_n; i += blockDim.x) a.cmb_cnt[i] = 0;
     __syncthreads();
     const int nt = c.misc[0];
-    const int U = RT * c.goff[nt];
+    // Phase 2 (one matrix) takes two 16-row tiles per unit, in the slots phase 1 uses for gate
+    // and up, when there are units enough for four per CTA even so: half the units, so half the
+    // per-unit hand-offs and reductions.
+    const bool pair2 = a.phase == 1 && (RT % 2) == 0 && RT * c.goff[nt] >= 8 * static_cast<int>(gridDim.x);
+    const int RTu = pair2 ? RT / 2 : RT;              // units per route group of an expert
+    const int TR = pair2 ? 2 * kRowTile : kRowTile;   // output rows per unit
+    const int nmat = (a.phase == 0 || pair2) ? 2 : 1;
+    const int U = RTu * c.goff[nt];
     const int u0 = static_cast<int>((static_cast<long long>(U) * blockIdx.x) / gridDim.x);
     const int u1 = static_cast<int>((static_cast<long long>(U) * (blockIdx.x + 1)) / gridDim.x);
     if (u0 >= u1) return;
 
     // Fused combine (phase 2 of a routed decode call), run by the compute warps and the
-    // reducer warp together once every unit of this CTA is stored: every unit bumps its 16-row
-    // tile's counter (over all CTAs); the CTA that completes a tile's count runs the
-    // slot-ordered combine of that tile.  Rounds of up to 32 units: the reducer bumps 32
-    // counters at once (one lane each) and lists the completed tiles, then all 17 warps
-    // combine them.
+    // reducer warps together once every unit of this CTA is stored: every unit bumps its row
+    // tile's counter (TR rows, over all CTAs); the CTA that completes a tile's count runs the
+    // slot-ordered combine of that tile.  Rounds of up to 32 units: the first reducer bumps 32
+    // counters at once (one lane each) and lists the completed tiles, then all compute and
+    // reducer warps combine them.
     auto fused_combine = [&]() {
         constexpr int kCmbThreads = (kNCW + kReducers) * 32;
         named_bar(2, kCmbThreads);                  // combine decision published
         if (!c.misc[2]) return;
         const int tix = warp < kNCW ? threadIdx.x : threadIdx.x - 32;     // skip the producer warp
-        const int per = a.T * kRowTile;
+        const int per = a.T * TR;
         const float* ev = static_cast<const float*>(a.out);
         int jl = 0;
         for (int ub = u0; ub < u1; ub += 32) {
@@ -277,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 int rt = 0, last = 0;
                 if (u < u1) {
                     int g;
-                    decode_unit(u, RT, c.goff, nt, jl, rt, g, c.cnt, tg);
+                    decode_unit(u, RTu, c.goff, nt, jl, rt, g, c.cnt, tg);
                     last = atomicAdd(a.cmb_cnt + rt, 1) + 1 == c.goff[nt];
                 }
                 const unsigned lm = __ballot_sync(0xffffffffu, last);
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             const int ntile = c.misc[3];
             for (int o = tix; o < ntile * per; o += kCmbThreads) {
                 const int tile = o / per, rem = o - tile * per;
-                const int t = rem / kRowTile, orow = c.ctile[tile] * kRowTile + rem % kRowTile;
+                const int t = rem / TR, orow = c.ctile[tile] * TR + rem % TR;
                 const size_t yo = static_cast<size_t>(t) * R + orow;
                 float accv = a.seed ? __ldcg(a.seed + yo) : 0.0f;
                 // products fetched four slots at a time, added in slot order
@@ -328,17 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         UnitCursor cu, cb;              // the unit being reduced, the unit whose bias is fetched
         auto step = [&](UnitCursor& x, int from) {     // x at unit `from` -> unit from + kReducers
             for (int q = 1; q <= kReducers; ++q)
-                if (from + q < u1) x.next(RT, c.goff);
+                if (from + q < u1) x.next(RTu, c.goff);
         };
         if (u0 + r < u1) {
-            cu.seek(u0 + r, RT, c.goff, nt);
+            cu.seek(u0 + r, RTu, c.goff, nt);
             cb = cu;
         }
         auto fetch_bias = [&]() {
-            const uint16_t* bp = lane < 16 ? a.b0 : (a.phase == 0 ? a.b1 : nullptr);
+            // phase 1: lanes 0-15 gate bias, 16-31 up bias of row `row`; phase 2: the down bias of
+            // row `row` of the unit's first (lanes 0-15) and, paired, second 16-row tile
+            const uint16_t* bp = lane < 16 ? a.b0 : (a.phase == 0 ? a.b1 : (pair2 ? a.b0 : nullptr));
             if (!bp) return 0.0f;
-            return __bfloat162float(__ushort_as_bfloat16(
-                bp[static_cast<size_t>(c.touched[cb.j]) * R + cb.rt * kRowTile + row]));
+            const int brow = cb.rt * TR + ((pair2 && lane >= 16) ? kRowTile : 0) + row;
+            return __bfloat162float(__ushort_as_bfloat16(bp[static_cast<size_t>(c.touched[cb.j]) * R + brow]));
         };
         float bias_next = u0 + r < u1 ? fetch_bias() : 0.0f;
         for (int u = u0 + r; u < u1; u += kReducers) {
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 }
             } else {
                 const float* redb = c.red + static_cast<size_t>(b) * kNCW * 2 * kRowTile * 8;
-                const int orow = rt * kRowTile + row;
+                const int orow = rt * TR + row;
                 for (int n = lane >> 4; n < cnt_g; n += 2) {
                     const int rid = a.dense ? rbase + n : PERM[rbase + n];
                     float s0 = 0.0f, s1 = 0.0f;
@@ -380,6 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                         static_cast<uint16_t*>(a.out)[static_cast<size_t>(rid) * R + orow] = float_to_adt_bits(h, a.adt);
                     } else {
                         static_cast<float*>(a.out)[static_cast<size_t>(rid) * R + orow] = s0;
+                        if (pair2)
+                            static_cast<float*>(a.out)[static_cast<size_t>(rid) * R + orow + kRowTile] = s1 * inv + bias1;
                     }
                 }
             }
@@ -401,13 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         int it = 0, slot = 0;
         uint32_t ph = 0;                // phase parity of the ring slot `slot`
         UnitCursor cu;
-        cu.seek(u0, RT, c.goff, nt);
+        cu.seek(u0, RTu, c.goff, nt);
         for (int u = u0; u < u1; ++u) {
-            if (u > u0) cu.next(RT, c.goff);
-            const int rt = cu.rt;
+            if (u > u0) cu.next(RTu, c.goff);
             const int e = c.touched[cu.j];
             for (int m = 0; m < nmat; ++m) {
-                const uint8_t* wbase = (m == 0 ? a.w0 : a.w1) + static_cast<size_t>(e) * a.mat_bytes;
+                // the m-th stream of the unit: gate / up (phase 1), or the m-th 16-row tile (phase 2)
+                const uint8_t* wbase = ((m == 0 || pair2) ? a.w0 : a.w1) + static_cast<size_t>(e) * a.mat_bytes;
+                const int rt = pair2 ? cu.rt * 2 + m : cu.rt;
                 for (int ch = 0; ch < nchunk; ++ch, ++it) {
                     const int s = slot;
                     const uint32_t par = ph ^ 1;
@@ -463,9 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     int staged_j = -1, staged_g = -1;
     const uint16_t* in = a.in;
     UnitCursor cu;
-    cu.seek(u0, RT, c.goff, nt);
+    cu.seek(u0, RTu, c.goff, nt);
     for (int u = u0; u < u1; ++u) {
-        if (u > u0) cu.next(RT, c.goff);
+        if (u > u0) cu.next(RTu, c.goff);
         const int j = cu.j, g = cu.g;
         const int e = c.touched[j];
         const int cnt_g = min(tg, c.cnt[j] - g * tg);
