@@ -204,7 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
     Carve c = carve(smem_raw, p, K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    pdl_wait();                 // inputs of this launch may come from the previous kernel
+    // Phase 2 starts before the launch ahead of it has finished: it begins only once every CTA
+    // of that launch has passed its own wait, so the route data are final by then, and weights
+    // are never written on the device.  The route tables and the weight ring fill at once; only
+    // the warps that read the hidden rows (or the combine's inputs) wait.
+    const bool early = a.phase == 1;
+    if (!early) pdl_wait();     // inputs of this launch may come from the previous kernel
     pdl_launch_dependents();
 
     // ---- route list (built here for decode sizes), unit tables --------------------------------
@@ -261,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int U = RTu * c.goff[nt];
     const int u0 = static_cast<int>((static_cast<long long>(U) * blockIdx.x) / gridDim.x);
     const int u1 = static_cast<int>((static_cast<long long>(U) * (blockIdx.x + 1)) / gridDim.x);
-    if (u0 >= u1) return;
+    if (u0 >= u1) {
+        if (early) pdl_wait();  // completes after the launch ahead of it, like every launch
+        return;
+    }
 
     // Fused combine (phase 2 of a routed decode call), run by the compute warps and the
     // reducer warps together once every unit of this CTA is stored: every unit bumps its row
@@ -274,8 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         named_bar(2, kCmbThreads);                  // combine decision published
         if (!c.misc[2]) return;
         const int tix = warp < kNCW ? threadIdx.x : threadIdx.x - 32;     // skip the producer warp
-        const int per = a.T * TR;
-        const float* ev = static_cast<const float*>(a.out);
         int jl = 0;
         for (int ub = u0; ub < u1; ub += 32) {
             if (warp == kNCW + 1) {
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 if (u < u1) {
                     int g;
                     decode_unit(u, RTu, c.goff, nt, jl, rt, g, c.cnt, tg);
-                    last = atomicAdd(a.cmb_cnt + rt, 1) + 1 == c.goff[nt];
+                    last = count_tile_unit(a.cmb_cnt, rt, c.goff[nt]);
                 }
                 const unsigned lm = __ballot_sync(0xffffffffu, last);
                 if (last) {
@@ -292,30 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     a.cmb_cnt[rt] = 0;                  // complete: ready for the next call
                 }
                 if (lane == 0) c.misc[3] = __popc(lm);
-                if (lm) __threadfence();
             }
             named_bar(2, kCmbThreads);              // tile list ready
             const int ntile = c.misc[3];
-            for (int o = tix; o < ntile * per; o += kCmbThreads) {
-                const int tile = o / per, rem = o - tile * per;
-                const int t = rem / TR, orow = c.ctile[tile] * TR + rem % TR;
-                const size_t yo = static_cast<size_t>(t) * R + orow;
-                float accv = a.seed ? __ldcg(a.seed + yo) : 0.0f;
-                // products fetched four slots at a time, added in slot order
-                for (int q0 = 0; q0 < a.k; q0 += 4) {
-                    float pv[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const size_t r = static_cast<size_t>(t) * a.k + q0 + q;
-                        pv[q] = q0 + q < a.k ? __fmul_rn(a.w[r], __ldcg(ev + r * R + orow)) : 0.0f;
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q0 + q < a.k) accv = __fadd_rn(accv, pv[q]);
-                }
-                if (a.y_f32) a.y_f32[yo] = accv;
-                static_cast<uint16_t*>(a.y)[yo] = float_to_adt_bits(accv, a.adt);
-            }
+            combine_tiles(a, c.ctile, ntile, TR, tix, kCmbThreads);
             named_bar(2, kCmbThreads);              // tile list consumed
         }
     };
@@ -329,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         // Every output this lane touches has row (lane & 15) of the tile, so the unit's biases
         // are fetched one unit ahead (lane l < 16: bias 0 of row l, lane 16 + l: bias 1) and
         // handed out with shuffles.
+        if (early) pdl_wait();
         const int r = warp - kNCW - 1;
         const int row = lane & 15;
         UnitCursor cu, cb;              // the unit being reduced, the unit whose bias is fetched
@@ -397,9 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             if (lane == 0) mbar_arrive(&c.rempty[b]);
         }
         if (a.cmb_mode == 2) {
-            // this CTA's outputs must be globally visible before it counts them
+            // the counting atomics (after the CTA barrier in the combine) release these outputs
             if (r == 0 && lane == 0) c.misc[2] = c.misc[1] == 0;
-            __threadfence();
             __syncwarp();
             fused_combine();
         }
@@ -468,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
 
     // ================================== consumer warps =========================================
+    if (early) pdl_wait();
     const int gid = lane >> 2, tid = lane & 3;
     int it = 0, slot = 0;
     uint32_t ph = 0;                    // phase parity of the ring slot `slot`

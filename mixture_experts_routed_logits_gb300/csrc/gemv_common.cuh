@@ -131,11 +131,12 @@ constexpr int kMaxLocalRoutes = 512;          // route lists built inside the ke
 // Route list for decode sizes (T*k <= 512, counting sort of the route ids by expert, ascending
 // id inside an expert, built by one warp) and the unit tables: touched experts in ascending
 // order, their route counts and the prefix of their route groups (groups of <= tg routes).
-// OFF is the route offsets to use (the in-kernel list when a.idx is set, else a.off).
+// The route offsets are the in-kernel list when a.idx is set, else a.off.  The
+// global route data are read past L1 (ld.global.cg): a phase-2 launch reads them before its
+// wait on the launch ahead of it.
 __device__ __forceinline__ void build_route_tables(const GemvArgs& a, int tg, int lane, int* off_s,
                                                    int* perm_s, int* tok_s, int* touched, int* cnt,
                                                    int* goff, int* misc) {
-    const int* OFF = a.idx ? off_s : a.off;
     if (a.idx) {
         // counting sort of the route ids by expert, ascending id inside an expert: chunks of
         // 32 routes, experts of a chunk grouped with match_any, one counter update per group
@@ -144,7 +145,7 @@ __device__ __forceinline__ void build_route_tables(const GemvArgs& a, int tg, in
 #pragma unroll
         for (int q = 0; q < kMaxLocalRoutes / 32; ++q) {
             const int r = q * 32 + lane;
-            ev[q] = r < n ? a.idx[r] : -1;
+            ev[q] = r < n ? __ldcg(a.idx + r) : -1;
         }
         for (int e = lane; e <= a.E; e += 32) off_s[e] = 0;
         __syncwarp();
@@ -215,7 +216,8 @@ __device__ __forceinline__ void build_route_tables(const GemvArgs& a, int tg, in
     } else {
         for (int e0 = 0; e0 < a.E; e0 += 32) {
             const int e = e0 + lane;
-            const int n = e < a.E ? OFF[e + 1] - OFF[e] : 0;
+            int n = 0;
+            if (e < a.E) n = a.idx ? off_s[e + 1] - off_s[e] : __ldcg(a.off + e + 1) - __ldcg(a.off + e);
             const unsigned m = __ballot_sync(0xffffffffu, n > 0);
             const int groups = n > 0 ? (n + tg - 1) / tg : 0;
             int incl = groups;
@@ -240,6 +242,82 @@ __device__ __forceinline__ void build_route_tables(const GemvArgs& a, int tg, in
         goff[nt] = acc;
         misc[0] = nt;
         misc[1] = 0;
+    }
+}
+
+// Counts one unit of row tile `tile` as done and says whether it was the tile's last (`need`
+// units).  The add is acq_rel at GPU scope: it releases this CTA's outputs (stored before a CTA
+// barrier that precedes the call) and, for the last unit, acquires every other CTA's.
+__device__ __forceinline__ bool count_tile_unit(int* cnt, int tile, int need) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(cnt + tile) : "memory");
+    return old + 1 == need;
+}
+
+// Slot-ordered combine of `ntile` completed row tiles of TR rows (tiles[i] * TR + 0..TR-1, every
+// token): y[t][row] = seed[t][row] + sum over slots q of w[t*k + q] * e[t*k + q][row], each
+// product rounded and then added in slot order.  A thread takes four consecutive rows of one
+// token (16-byte loads and stores) and two such quads per round, with all their loads issued
+// before any is used: the CTA that completes the last tiles does this alone, so its latency is
+// the call's tail.  TR and R are multiples of 4; e and the seed sit in the 256-byte aligned
+// workspace and y, y_f32 are 16-byte aligned (the entry point refuses them otherwise).
+__device__ __forceinline__ void combine_tiles(const GemvArgs& a, const int* tiles, int ntile, int TR,
+                                              int tix, int nthr) {
+    constexpr int kU = 2;
+    const int R = a.R, TQ = TR / 4;
+    const int per = a.T * TQ, total = ntile * per;
+    const float* ev = static_cast<const float*>(a.out);
+    uint16_t* y = static_cast<uint16_t*>(a.y);
+    auto ld4 = [](const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); };
+    for (int o0 = tix; o0 < total; o0 += kU * nthr) {
+        float4 acc[kU];
+        size_t yo[kU];
+        int orow[kU], rk[kU];
+        bool v[kU];
+#pragma unroll
+        for (int i = 0; i < kU; ++i) {
+            const int o = o0 + i * nthr;
+            v[i] = o < total;
+            const int oo = v[i] ? o : 0;
+            const int tile = oo / per, rem = oo - tile * per;
+            const int t = rem / TQ;
+            orow[i] = tiles[tile] * TR + (rem - t * TQ) * 4;
+            rk[i] = t * a.k;
+            yo[i] = static_cast<size_t>(t) * R + orow[i];
+            acc[i] = (v[i] && a.seed) ? ld4(a.seed + yo[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int q0 = 0; q0 < a.k; q0 += 4) {
+            float4 ex[kU][4];
+            float wq[kU][4];
+#pragma unroll
+            for (int i = 0; i < kU; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const bool use = v[i] && q0 + q < a.k;
+                    const int r = rk[i] + q0 + q;
+                    wq[i][q] = use ? a.w[r] : 0.0f;
+                    ex[i][q] = use ? ld4(ev + static_cast<size_t>(r) * R + orow[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int i = 0; i < kU; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (q0 + q >= a.k) continue;
+                    acc[i].x = __fadd_rn(acc[i].x, __fmul_rn(wq[i][q], ex[i][q].x));
+                    acc[i].y = __fadd_rn(acc[i].y, __fmul_rn(wq[i][q], ex[i][q].y));
+                    acc[i].z = __fadd_rn(acc[i].z, __fmul_rn(wq[i][q], ex[i][q].z));
+                    acc[i].w = __fadd_rn(acc[i].w, __fmul_rn(wq[i][q], ex[i][q].w));
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < kU; ++i) {
+            if (!v[i]) continue;
+            const uint16_t b0 = float_to_adt_bits(acc[i].x, a.adt), b1 = float_to_adt_bits(acc[i].y, a.adt);
+            const uint16_t b2 = float_to_adt_bits(acc[i].z, a.adt), b3 = float_to_adt_bits(acc[i].w, a.adt);
+            if (a.y_f32) *reinterpret_cast<float4*>(a.y_f32 + yo[i]) = acc[i];
+            *reinterpret_cast<uint2*>(y + yo[i]) =
+                make_uint2(b0 | (static_cast<uint32_t>(b1) << 16), b2 | (static_cast<uint32_t>(b3) << 16));
+        }
     }
 }
 

@@ -558,13 +558,10 @@ __global__ void __launch_bounds__(kThr, 1) gemv_sk_kernel(const __grid_constant_
 
     // ---- fused combine (phase 2 of a routed decode call) -------------------------------------
     if (a.cmb_mode == 2) {
-        // this CTA's outputs must be globally visible before it counts them
-        __threadfence();
+        // every output of this CTA is stored before the barrier; the counting atomics release them
         if (warp == 0 && lane == 0) c.misc[2] = c.misc[1] == 0;
         named_bar(2, kThr);
         if (c.misc[2]) {
-            const int per = a.T * kRowTile;
-            const float* ev = static_cast<const float*>(a.out);
             SkCursor cc;
             cc.seek(u0, RT, c.goff, nt);
             for (int ub = u0; ub < u1; ub += 32) {
@@ -575,7 +572,7 @@ __global__ void __launch_bounds__(kThr, 1) gemv_sk_kernel(const __grid_constant_
                     for (int q = 0; q < lane && ub + q + 1 < u1; ++q) lc.next(RT, c.goff);
                     if (ub + lane < u1) {
                         rt = lc.rt;
-                        last = atomicAdd(a.cmb_cnt + rt, 1) + 1 == c.goff[nt];
+                        last = count_tile_unit(a.cmb_cnt, rt, c.goff[nt]);
                     }
                     const unsigned lm = __ballot_sync(0xffffffffu, last);
                     if (last) {
@@ -583,31 +580,11 @@ __global__ void __launch_bounds__(kThr, 1) gemv_sk_kernel(const __grid_constant_
                         a.cmb_cnt[rt] = 0;              // complete: ready for the next call
                     }
                     if (lane == 0) c.misc[3] = __popc(lm);
-                    if (lm) __threadfence();
                 }
                 for (int q = 0; q < 32 && ub + q + 1 < u1; ++q) cc.next(RT, c.goff);
                 named_bar(2, kThr);              // tile list ready
                 const int ntile = c.misc[3];
-                for (int o = threadIdx.x; o < ntile * per; o += kThr) {
-                    const int tile = o / per, rem = o - tile * per;
-                    const int t = rem / kRowTile, orow = c.ctile[tile] * kRowTile + rem % kRowTile;
-                    const size_t yo = static_cast<size_t>(t) * R + orow;
-                    float accv = a.seed ? __ldcg(a.seed + yo) : 0.0f;
-                    // products fetched four slots at a time, added in slot order
-                    for (int q0 = 0; q0 < a.k; q0 += 4) {
-                        float pv[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const size_t r = static_cast<size_t>(t) * a.k + q0 + q;
-                            pv[q] = q0 + q < a.k ? __fmul_rn(a.w[r], __ldcg(ev + r * R + orow)) : 0.0f;
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (q0 + q < a.k) accv = __fadd_rn(accv, pv[q]);
-                    }
-                    if (a.y_f32) a.y_f32[yo] = accv;
-                    static_cast<uint16_t*>(a.y)[yo] = float_to_adt_bits(accv, a.adt);
-                }
+                combine_tiles(a, c.ctile, ntile, kRowTile, threadIdx.x, kThr);
                 named_bar(2, kThr);              // tile list consumed
             }
         }

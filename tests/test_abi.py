@@ -72,6 +72,14 @@ def test_forward_rejects_small_workspace_and_nulls(L):
     args[0] = ctypes.c_void_p(0x2000)
     args[6] = 33                       # k > E
     assert L.ts_moe_forward(*args) == 1
+    args[6] = 4
+    args[8] = ctypes.c_void_p(0x5008)  # y not 16-byte aligned
+    assert L.ts_moe_forward(*args) == 1
+    assert b"aligned" in L.ts_last_error()
+    args[8] = ctypes.c_void_p(0x5000)
+    args[9] = ctypes.c_void_p(0x7004)  # y_f32 not 16-byte aligned
+    assert L.ts_moe_forward(*args) == 1
+    args[9] = None
     bf = _experts(fmt=1)
     a2 = list(args)
     a2[6] = 4
