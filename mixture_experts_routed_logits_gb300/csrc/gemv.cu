@@ -187,6 +187,15 @@ __device__ __forceinline__ void decode_unit(int u, int RT, const int* goff, int 
     g = local % ng;
 }
 
+// Block slot of compute warp w (a permutation of 0..15): warps 0,4,8,12 (sub-partition 0, with
+// the producer warp 16) -> 10..13; 1,5,9,13 (with reducer 17) -> 14,0,1,2; 2,6,10,14 (with
+// reducer 18) -> 15,3,4,5; 3,7,11,15 -> 6..9.
+static_assert(kNCW == 16 && kReducers == 2, "block slot table assumes 16 compute warps, 2 reducers");
+__device__ __forceinline__ int block_slot(int w) {
+    constexpr uint64_t kSlots = 0x952D841C730B6FEAull;   // nibble w = slot of warp w
+    return static_cast<int>((kSlots >> (4 * w)) & 15u);
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ KParams P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -398,9 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         uint32_t ph = 0;                // phase parity of the ring slot `slot`
         UnitCursor cu;
         cu.seek(u0, RTu, c.goff, nt);
+        int pj = -1, e = 0;
         for (int u = u0; u < u1; ++u) {
             if (u > u0) cu.next(RTu, c.goff);
-            const int e = c.touched[cu.j];
+            if (cu.j != pj) {
+                pj = cu.j;
+                e = c.touched[pj];
+            }
             for (int m = 0; m < nmat; ++m) {
                 // the m-th stream of the unit: gate / up (phase 1), or the m-th 16-row tile (phase 2)
                 const uint8_t* wbase = ((m == 0 || pair2) ? a.w0 : a.w1) + static_cast<size_t>(e) * a.mat_bytes;
@@ -458,54 +471,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int gid = lane >> 2, tid = lane & 3;
     int it = 0, slot = 0;
     uint32_t ph = 0;                    // phase parity of the ring slot `slot`
-    int staged_j = -1, staged_g = -1;
     const uint16_t* in = a.in;
+    // The route group's row mapping is looked up (and, outside token mode, its activations
+    // staged) only when the group changes: consecutive units mostly share it, only the row tile
+    // moves, so a unit's first fragment load does not wait on a chain of shared-memory lookups.
+    int ckey = -1;                      // (j << 16) | g of the current group
+    int brow = 0, xc0 = 0, xc1 = 0;     // activation row this lane feeds the mma; INT4 x-sum columns
+    float my_rinv = 0.0f;               // warp 0, lane n < 8: inverse prescale of column n
     UnitCursor cu;
     cu.seek(u0, RTu, c.goff, nt);
     for (int u = u0; u < u1; ++u) {
         if (u > u0) cu.next(RTu, c.goff);
-        const int j = cu.j, g = cu.g;
-        const int e = c.touched[j];
-        const int cnt_g = min(tg, c.cnt[j] - g * tg);
-        const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
-        // staged row of each of the unit's columns (routes): the token in token mode
-        auto row_of = [&](int n) {
-            if (!tokmode) return n < tg ? n : 0;
-            if (n >= cnt_g) return 0;
-            if (a.dense) return rbase + n;
-            return a.idx ? c.tok_s[rbase + n] : PERM[rbase + n] / a.k;
-        };
-        const int brow = row_of(gid);                 // activation row this lane feeds the mma
-        const int xc0 = row_of(2 * tid), xc1 = row_of(2 * tid + 1);   // INT4 x-sum columns
-
-        // ---- stage this group's activations (f16 with prescale, or as-is) -----------------
-        if (!tokmode && (j != staged_j || g != staged_g)) {
-            // every compute warp must be done with the previous group's activations
-            if (staged_j >= 0) named_bar(1, kNCW * 32);
-            staged_j = j;
-            staged_g = g;
-            if (warp < 8) {
-                const int n = warp;
-                float inv = 0.0f;
-                if (n < cnt_g) {
-                    const int rid = a.dense ? rbase + n : PERM[rbase + n];
-                    size_t row;
-                    if (a.phase == 0) row = a.dense ? static_cast<size_t>(rid) : static_cast<size_t>(rid / a.k);
-                    else row = static_cast<size_t>(rid);
-                    inv = stage_row<FMT>(in + row * K, c.xs + static_cast<size_t>(n) * p.xstride, c.xsum, n,
-                                         K, nblk, prescale, copy_bits, lane);
-                } else {
-                    if (n < tg) {
-                        unsigned char* xrow = c.xs + static_cast<size_t>(n) * p.xstride;
-                        for (int q = lane; q < K / 8; q += 32)
-                            reinterpret_cast<uint4*>(xrow)[q] = make_uint4(0, 0, 0, 0);
-                    }
-                    if (FMT == FMT_INT4)
-                        for (int blk = lane; blk < nblk; blk += 32) c.xsum[blk * 8 + n] = 0.0f;
-                }
-                if (lane == 0) c.xinv[n] = inv;
+        const int key = (cu.j << 16) | cu.g;
+        if (key != ckey) {
+            const bool first = ckey < 0;
+            ckey = key;
+            const int j = cu.j, g = cu.g;
+            const int e = c.touched[j];
+            const int cnt_g = min(tg, c.cnt[j] - g * tg);
+            const int rbase = a.dense ? g * tg : OFF[e] + g * tg;
+            // staged row of each of the unit's columns (routes): the token in token mode
+            auto row_of = [&](int n) {
+                if (!tokmode) return n < tg ? n : 0;
+                if (n >= cnt_g) return 0;
+                if (a.dense) return rbase + n;
+                return a.idx ? c.tok_s[rbase + n] : PERM[rbase + n] / a.k;
+            };
+            brow = row_of(gid);
+            if (FMT == FMT_INT4) {
+                xc0 = row_of(2 * tid);
+                xc1 = row_of(2 * tid + 1);
             }
-            named_bar(1, kNCW * 32);
+            // ---- stage this group's activations (f16 with prescale, or as-is) -------------
+            if (!tokmode) {
+                // every compute warp must be done with the previous group's activations
+                if (!first) named_bar(1, kNCW * 32);
+                if (warp < 8) {
+                    const int n = warp;
+                    float inv = 0.0f;
+                    if (n < cnt_g) {
+                        const int rid = a.dense ? rbase + n : PERM[rbase + n];
+                        size_t row;
+                        if (a.phase == 0) row = a.dense ? static_cast<size_t>(rid) : static_cast<size_t>(rid / a.k);
+                        else row = static_cast<size_t>(rid);
+                        inv = stage_row<FMT>(in + row * K, c.xs + static_cast<size_t>(n) * p.xstride, c.xsum, n,
+                                             K, nblk, prescale, copy_bits, lane);
+                    } else {
+                        if (n < tg) {
+                            unsigned char* xrow = c.xs + static_cast<size_t>(n) * p.xstride;
+                            for (int q = lane; q < K / 8; q += 32)
+                                reinterpret_cast<uint4*>(xrow)[q] = make_uint4(0, 0, 0, 0);
+                        }
+                        if (FMT == FMT_INT4)
+                            for (int blk = lane; blk < nblk; blk += 32) c.xsum[blk * 8 + n] = 0.0f;
+                    }
+                    if (lane == 0) c.xinv[n] = inv;
+                }
+                named_bar(1, kNCW * 32);
+            }
+            if (warp == 0 && lane < 8) my_rinv = c.xinv[row_of(lane)];
         }
 
         // ---- stream the unit's weight chunks ---------------------------------------------------
@@ -588,14 +612,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                             ac[3] += d[3];
                         }
                     };
-                    // three blocks in flight per warp: independent fragments, interleavable
-                    int i = warp;
+                    // three blocks in flight per warp: independent fragments, interleavable; the
+                    // ragged rest (at most two blocks) also in one round.  Warp w starts at block
+                    // slot block_slot(w): when a stage splits unevenly, the warps that share an SM
+                    // sub-partition with the producer (w % 4 == 0) or a reducer (w % 4 == 1, 2)
+                    // get the highest slots, which have one block fewer.
+                    int i = block_slot(warp);
                     for (; i + 2 * kNCW < nbc; i += 3 * kNCW) {
                         block(i);
                         block(i + kNCW);
                         block(i + 2 * kNCW);
                     }
-                    for (; i < nbc; i += kNCW) block(i);
+                    if (i < nbc) {
+                        block(i);
+                        if (i + kNCW < nbc) block(i + kNCW);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&c.empty[s]);
@@ -622,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 rm[(gid + 8) * 8 + 2 * tid] = acc[m][2];
                 rm[(gid + 8) * 8 + 2 * tid + 1] = acc[m][3];
             }
-            if (warp == 0 && lane < 8) c.rinv[b * 8 + lane] = c.xinv[row_of(lane)];
+            if (warp == 0 && lane < 8) c.rinv[b * 8 + lane] = my_rinv;
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.rfull[b]);
         }
