@@ -170,7 +170,12 @@ ts_status ts_moe_router_route(const void* x, int32_t adt, int32_t T, int32_t H, 
  *   off   device int32 [E+1] out: off[e] = number of routes to experts below e
  *   perm  device int32 [T*k] out: route ids grouped by expert, ascending id within an expert
  *   inv   device int32 [T*k] out: inv[r] = position of route r in perm
- * Bit-exact (integer work).  Rejects T*k > 2^24.                                          */
+ * Bit-exact (integer work).  Rejects T*k > 2^24.
+ * A route whose expert id lies outside 0..E-1 is left out (inv[r] = -1; inside
+ * ts_moe_forward it also sets TS_ERR_INVALID_ARG in the device status word), and perm
+ * positions off[E]..T*k-1 hold route id 0.  Whatever idx holds, even if it changes while the
+ * kernel runs, every perm entry is a route id in 0..T*k-1, so the kernels that read the list
+ * stay inside their buffers.                                                              */
 ts_status ts_moe_build_routes(const int32_t* idx, int32_t T, int32_t E, int32_t k, int32_t* off,
                               int32_t* perm, int32_t* inv, void* stream);
 

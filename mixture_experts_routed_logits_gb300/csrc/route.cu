@@ -372,6 +372,13 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
     pdl_wait();                 // idx comes from the previous kernel
     pdl_launch_dependents();
     for (int e = tid; e < E; e += kBuildThreads) cnt[e] = 0;
+    // Every position starts as a valid route id and every route as unplaced, so that the list
+    // stays inside 0..n-1 even if idx holds ids outside 0..E-1 or changes between the two
+    // passes below (the placement never leaves an expert's counted range).
+    for (int r = tid; r < n; r += kBuildThreads) {
+        perm[r] = 0;
+        inv[r] = -1;
+    }
     __syncthreads();
     for (int r = tid; r < n; r += kBuildThreads) {
         const int e = idx[r];
@@ -385,6 +392,7 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
             off[e] = acc;
             cursor[e] = acc;
             acc += cnt[e];
+            cnt[e] = acc;               // end of expert e's range
         }
         off[E] = acc;
     }
@@ -406,8 +414,12 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
         if (e >= 0) {
             int pos = cursor[e] + rank;
             for (int w2 = 0; w2 < warp; ++w2) pos += wcnt[w2][e];
-            perm[pos] = r;
-            inv[r] = pos;
+            if (pos < cnt[e]) {
+                perm[pos] = r;
+                inv[r] = pos;
+            } else {
+                report_error(status, DEV_ERR_INVALID);   // idx changed since it was counted
+            }
         }
         __syncthreads();
         for (int e2 = tid; e2 < E; e2 += kBuildThreads) {

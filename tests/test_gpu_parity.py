@@ -167,6 +167,39 @@ def test_forward_deterministic(case):
     assert moe.device_status(ws) == 0
 
 
+@pytest.mark.parametrize("path,T", [("gemm", 300), ("gemv", 300), ("auto", 8)])
+def test_expert_ids_out_of_range_are_reported_and_stay_in_bounds(path, T):
+    """Routes to expert ids outside 0..E-1 are left out and reported through the device status
+    word (TS_ERR_INVALID_ARG); the call completes, the route list stays inside 0..T*k-1 and
+    the routes of valid ids are placed exactly as the oracle places them."""
+    moe = _moe()
+    cfg, shapes = 5, dict(H=256, I=512, E=8, k=2)
+    L, D = _make(cfg, T, shapes)
+    c = L["cfg"]
+    rng = np.random.default_rng(7)
+    idx = np.stack([rng.choice(c["E"], size=c["k"], replace=False) for _ in range(T)]).astype(np.int32)
+    bad = rng.choice(T * c["k"], size=5, replace=False)
+    idx.reshape(-1)[bad] = np.array([-1, c["E"], 1 << 20, -(1 << 30), c["E"] + 3], np.int32)
+    w = np.full((T, c["k"]), 0.5, np.float32)
+    ex, sh = gpu_layer(D)
+    ws = moe.alloc_workspace(T, c["k"], ex, sh)
+    y, _ = moe.forward(D["x"], ex, torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), ws=ws, path=path)
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 1
+    off, perm, inv = moe.build_routes(torch.from_numpy(idx).cuda(), c["E"])
+    torch.cuda.synchronize()
+    off, perm, inv = off.cpu().numpy(), perm.cpu().numpy(), inv.cpu().numpy()
+    assert perm.min() >= 0 and perm.max() < T * c["k"]
+    assert np.all(inv[bad] == -1)
+    good = np.setdiff1d(np.arange(T * c["k"]), bad)
+    assert off[-1] == good.size
+    # the valid routes grouped by expert, ascending id within an expert, then route id 0
+    order = good[np.argsort(idx.reshape(-1)[good], kind="stable")]
+    assert np.array_equal(perm[:good.size], order)
+    assert np.all(perm[good.size:] == 0)
+    assert np.array_equal(inv[order], np.arange(good.size))
+
+
 def test_forward_empty_batch_launches_nothing():
     moe = _moe()
     L, D = _make(1, 4, None)
