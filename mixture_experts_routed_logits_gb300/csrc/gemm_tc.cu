@@ -25,9 +25,10 @@
 //     thread, tcgen05.mma kind::f16, 128B-swizzled K-major smem descriptors), warps 2-5 =
 //     epilogue (tcgen05.ld of their TMEM lane quarter).  Every mbarrier wait is bounded.
 //   * MXFP4 weights (QUANT variant): the producer bulk-copies the packed e2m1 tiles (with their
-//     e8m0 block scales) into a staging area of each stage; four dequant warps turn them into
-//     f16 (hardware e2m1x2 -> f16x2 convert, times the block scale, exact while the scale is in
-//     [2^-23, 2^13]; outside it the device status reports TS_ERR_UNSUPPORTED) written straight into the 128B-swizzled A tile; the MMA waits on a
+//     e8m0 block scales) into a staging area of each stage; sixteen dequant warps turn them
+//     into f16 (hardware e2m1x2 -> f16x2 convert, times the block scale, exact while the scale
+//     is in [2^-23, 2^13]; outside it the device status reports TS_ERR_UNSUPPORTED) written
+//     straight into the 128B-swizzled A tile (two A stages); the MMA waits on a
 //     "dequantised" barrier instead of the copy barrier.  Activations enter as f16 with a
 //     per-route power-of-two prescale that the epilogue undoes.  Each weight element crosses HBM
 //     once per route tile, as packed bytes.
@@ -49,8 +50,9 @@ constexpr int kThreads = 192;
 // QUANT variant: a packed slot holds the B boxes and two 8-row-tile x 2-block packed tiles
 constexpr int kPackBlk = 272;
 constexpr int kStaging = 2 * 8 * 2 * kPackBlk;             // 8704 B
-constexpr int kThreadsQ = 448;                              // + 8 dequant warps
-constexpr int kDqWarps = 8;
+constexpr int kDqWarps = 16;                                // dequant warps (8 or 16)
+constexpr int kThreadsQ = kThreads + 32 * kDqWarps;
+static_assert(kDqWarps == 8 || kDqWarps == 16, "the dequant split covers 32 blocks per stage");
 
 struct TcLayout {        // host-chosen shape of one launch
     int bn;              // routes per tile (64 or 256)
@@ -380,12 +382,14 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 }
                 const unsigned char* stg = ring + static_cast<size_t>(s) * Ly.slot_bytes + bbytes;
                 unsigned char* adst = base + sa * 2 * kATile;
-                // this warp: block column bb = dw & 1 of row tiles (dw >> 1) and (dw >> 1) + 4 of
-                // both tiles; the 128B swizzle puts 16-byte chunk c of row r at c ^ (r & 7)
+                // this warp: block column bb = dw & 1 of row tiles (dw >> 1) + (kDqWarps / 2) * g
+                // (g < 16 / kDqWarps) of both tiles; the 128B swizzle puts 16-byte chunk c of row
+                // r at c ^ (r & 7)
+                constexpr int kPer = 32 / kDqWarps;       // blocks per warp and stage
 #pragma unroll
-                for (int qi = 0; qi < 4; ++qi) {
-                    const int tile = qi >> 1;
-                    const int rt = (dw >> 1) + 4 * (qi & 1);
+                for (int qi = 0; qi < kPer; ++qi) {
+                    const int tile = qi / (kPer / 2);
+                    const int rt = (dw >> 1) + (kDqWarps / 2) * (qi % (kPer / 2));
                     // row tiles past the matrix only feed output rows that are never stored
                     if ((tile == 0 ? rt0 : rt1) + rt >= RTm) continue;
                     const unsigned char* blk = stg + (tile * 8 + rt) * 2 * kPackBlk + bb * kPackBlk;
