@@ -55,7 +55,7 @@ constexpr int kThreadsQ = kThreads + 32 * kDqWarps;
 static_assert(kDqWarps == 8 || kDqWarps == 16, "the dequant split covers 32 blocks per stage");
 
 struct TcLayout {        // host-chosen shape of one launch
-    int bn;              // routes per tile (64 or 256)
+    int bn;              // routes per tile (64, 128 or 256; <= 128 double-buffers TMEM)
     int nslot;           // stages (16-bit weights) or packed slots (MXFP4)
     int slot_bytes;      // bytes per stage / slot (multiple of 1024)
     int a_ring_bytes;    // MXFP4: two dequantised A stages (64 KB); else 0
@@ -170,8 +170,8 @@ struct SmemTail {
     uint64_t empty[kMaxSlots];      // stage / packed slot consumed by the MMA
     uint64_t afull[2];              // QUANT: dequantised A stage written
     uint64_t aempty[2];             // QUANT: dequantised A stage consumed by the MMA
-    uint64_t tfull;
-    uint64_t tempty;
+    uint64_t tfull[2];              // accumulator set b holds a finished item
+    uint64_t tempty[2];             // accumulator set b read out by the epilogue
     uint32_t tmem_base;
     volatile int abort_flag;
     int nt;                         // touched experts
@@ -199,6 +199,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     const int MB = (R + rows_per_item - 1) / rows_per_item;
     const int nkb = K / kBK;
     const int NS = Ly.nslot, BN = Ly.bn, S = Ly.S;
+    // Accumulator sets in the 512 TMEM columns: tiles of <= 128 routes use two sets of (gate,
+    // up) or (rows, rows + 128) at columns 0 / 128 and 256 / 384, alternating per item, so the
+    // MMAs of an item run while the epilogue drains the one before; wider tiles use one set at
+    // columns 0 and 256.
+    const int NB = BN <= 128 ? 2 : 1;
+    const uint32_t acc1 = NB == 2 ? 128u : 256u;      // column of the second accumulator
     const int kbp = (nkb + S - 1) / S;                      // stages per K part
     const int bbytes = (BN / 64) * kBBox;                   // B area of a stage / slot
 
@@ -229,12 +235,14 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             mbar_init(&tl->afull[s], kDqWarps);
             mbar_init(&tl->aempty[s], 1);
         }
-        mbar_init(&tl->tfull, 1);
-        mbar_init(&tl->tempty, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tl->tfull[b], 1);
+            mbar_init(&tl->tempty[b], 4);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
-        // 512 TMEM columns: accumulator 0 at column 0, accumulator 1 at column 256
+        // 512 TMEM columns: one or two accumulator sets (see NB above)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
                          smem_u32(&tl->tmem_base))
                      : "memory");
@@ -318,7 +326,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 const int N = (n_valid + 15) & ~15;
                 const uint32_t idesc = idesc_f16kind(a.ab_bf16, kBM, N);
                 const int kb0 = kp * kbp, kb1 = min(nkb, kb0 + kbp);
-                if (!mbar_wait_bounded(&tl->tempty, (n_item & 1) ^ 1)) {
+                const int tb = n_item % NB, tuse = n_item / NB;
+                const uint32_t tset = tmem + static_cast<uint32_t>(tb) * 256u;
+                if (!mbar_wait_bounded(&tl->tempty[tb], (tuse & 1) ^ 1)) {
                     tl->abort_flag = 1;
                     report_error(a.status, DEV_ERR_TIMEOUT);
                     break;
@@ -344,14 +354,14 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks) {
                         const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
-                        umma(tmem, d0 + 2 * ks, db + 2 * ks, idesc, acc);
-                        umma(tmem + 256, d1 + 2 * ks, db + 2 * ks, idesc, acc);
+                        umma(tset, d0 + 2 * ks, db + 2 * ks, idesc, acc);
+                        umma(tset + acc1, d1 + 2 * ks, db + 2 * ks, idesc, acc);
                     }
                     umma_commit(&tl->empty[s]);         // frees the slot once these MMAs are done
                     if (QUANT) umma_commit(&tl->aempty[sa]);
                 }
                 if (!ok) break;
-                umma_commit(&tl->tfull);                // accumulators ready for the epilogue
+                umma_commit(&tl->tfull[tb]);            // accumulators ready for the epilogue
             }
         }
     } else if (QUANT && warp >= 6) {
@@ -443,7 +453,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             const int p0 = a.off[e] + tile * tl->bnj[j];
             const int n_valid = min(tl->bnj[j], tl->cnt[j] - tile * tl->bnj[j]);
             const int N = (n_valid + 15) & ~15;
-            bool ok = !tl->abort_flag && mbar_wait_bounded(&tl->tfull, n_item & 1);
+            const int tb = n_item % NB, tuse = n_item / NB;
+            const uint32_t tqs = tq + static_cast<uint32_t>(tb) * 256u;   // this item's set
+            bool ok = !tl->abort_flag && mbar_wait_bounded(&tl->tfull[tb], tuse & 1);
             if (!ok) {
                 if (lane == 0) {
                     tl->abort_flag = 1;
@@ -470,7 +482,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             if (S == 1) {
                 for (int c0 = 0; c0 < N; c0 += 16) {
                     float d0[16], d1[16];
-                    tmem_ld16_pair(tq + c0, tq + 256 + c0, d0, d1);
+                    tmem_ld16_pair(tqs + c0, tqs + acc1 + c0, d0, d1);
                     if (a.phase == 0) {
 #pragma unroll
                         for (int t = 0; t < 16; ++t) {
@@ -502,14 +514,14 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tl->tempty);
+                if (lane == 0) mbar_arrive(&tl->tempty[tb]);
                 continue;
             }
             // split K: park this part's accumulators, the group's last part finishes
             float* part = a.part;
             for (int c0 = 0; c0 < N; c0 += 16) {
                 float d0[16], d1[16];
-                tmem_ld16_pair(tq + c0, tq + 256 + c0, d0, d1);
+                tmem_ld16_pair(tqs + c0, tqs + acc1 + c0, d0, d1);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int c = c0 + t;
@@ -521,7 +533,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tl->tempty);     // TMEM is free again
+            if (lane == 0) mbar_arrive(&tl->tempty[tb]);   // this set is free again
             // each warp owns its 32-row slice: one counter per (group, slice), so no barrier
             // between the epilogue warps is needed
             __threadfence();
@@ -728,7 +740,10 @@ cudaError_t launch_h_to_f16(const uint16_t* h, int adt, int I, int n, uint16_t* 
 static TcLayout tc_layout(const GemmArgs& a, int num_sms, size_t* smem) {
     TcLayout L{};
     const int Tk = a.rows_in;
-    L.bn = Tk <= 256 ? 64 : 256;
+    // MXFP4 calls take 128-route tiles: the epilogue of one item then overlaps the next item's
+    // MMAs (two accumulator sets), which outweighs re-dequantising the weights of experts with
+    // more than 128 routes
+    L.bn = Tk <= 256 ? 64 : (a.quant ? 128 : 256);
     // shared-memory tail (barriers and the item tables) plus 1 KB for aligning the base to 1024
     constexpr size_t kTailBytes = (sizeof(SmemTail) + 255) / 256 * 256;
     const size_t tail = kTailBytes + 1024;
