@@ -614,6 +614,64 @@ __device__ __forceinline__ float block_max128(float v, float* red) {
     return m;
 }
 
+// One row of n 16-bit values (n % 8 == 0, both pointers 16-byte aligned) to f16 times 2^ks with
+// max |v| * 2^ks in [2^14, 2^15) (prescale_of); returns 2^-ks.  A 128-thread block moves the row
+// in 16-byte pieces; rows of up to 128 * 8 * kRowV elements are read once and kept in registers
+// between the max and the conversion, longer rows are read twice.
+constexpr int kRowV = 4;
+__device__ __forceinline__ float row_to_f16(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                            int n, int adt, float* red) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    const int nv = n / 8;
+    auto absmax8 = [&](const uint4& v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float m = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            m = fmaxf(m, fabsf(adt_bits_to_float(static_cast<uint16_t>(w[h] & 0xFFFF), adt)));
+            m = fmaxf(m, fabsf(adt_bits_to_float(static_cast<uint16_t>(w[h] >> 16), adt)));
+        }
+        return m;
+    };
+    auto conv8 = [&](const uint4& v, float scl) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const uint32_t lo = __half_as_ushort(__float2half_rn(
+                __fmul_rn(adt_bits_to_float(static_cast<uint16_t>(w[h] & 0xFFFF), adt), scl)));
+            const uint32_t hi = __half_as_ushort(__float2half_rn(
+                __fmul_rn(adt_bits_to_float(static_cast<uint16_t>(w[h] >> 16), adt), scl)));
+            o[h] = lo | (hi << 16);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    float mx = 0.0f, scl, inv;
+    if (nv <= kRowV * 128) {
+        uint4 v[kRowV];
+#pragma unroll
+        for (int q = 0; q < kRowV; ++q) {
+            const int i = threadIdx.x + 128 * q;
+            v[q] = i < nv ? __ldg(s4 + i) : make_uint4(0u, 0u, 0u, 0u);
+            mx = fmaxf(mx, absmax8(v[q]));
+        }
+        mx = block_max128(mx, red);
+        prescale_of(mx, scl, inv);
+#pragma unroll
+        for (int q = 0; q < kRowV; ++q) {
+            const int i = threadIdx.x + 128 * q;
+            if (i < nv) d4[i] = conv8(v[q], scl);
+        }
+    } else {
+        for (int i = threadIdx.x; i < nv; i += 128) mx = fmaxf(mx, absmax8(__ldg(s4 + i)));
+        mx = block_max128(mx, red);
+        prescale_of(mx, scl, inv);
+        for (int i = threadIdx.x; i < nv; i += 128) d4[i] = conv8(__ldg(s4 + i), scl);
+    }
+    return inv;
+}
+
 // Route-ordered activations for the f16 tensor-core operand: xs[p] = f16(x[perm[p]/k] * 2^ks),
 // inv[p] = 2^-ks.
 __global__ void __launch_bounds__(128) gather_rows_f16_kernel(const uint16_t* __restrict__ x, int adt,
@@ -625,15 +683,8 @@ __global__ void __launch_bounds__(128) gather_rows_f16_kernel(const uint16_t* __
     pdl_launch_dependents();
     const int p = blockIdx.x;
     if (p >= n) return;
-    const uint16_t* src = x + static_cast<size_t>(perm[p] / k) * H;
-    float mx = 0.0f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) mx = fmaxf(mx, fabsf(adt_bits_to_float(src[i], adt)));
-    mx = block_max128(mx, red);
-    float scl, inv;
-    prescale_of(mx, scl, inv);
-    uint16_t* dst = xs + static_cast<size_t>(p) * H;
-    for (int i = threadIdx.x; i < H; i += blockDim.x)
-        dst[i] = __half_as_ushort(__float2half_rn(__fmul_rn(adt_bits_to_float(src[i], adt), scl)));
+    const float inv = row_to_f16(x + static_cast<size_t>(perm[p] / k) * H, xs + static_cast<size_t>(p) * H,
+                                 H, adt, red);
     if (threadIdx.x == 0) inv_out[p] = inv;
 }
 
@@ -646,15 +697,7 @@ __global__ void __launch_bounds__(128) h_to_f16_kernel(const uint16_t* __restric
     pdl_launch_dependents();
     const int p = blockIdx.x;
     if (p >= n) return;
-    const uint16_t* src = h + static_cast<size_t>(p) * I;
-    float mx = 0.0f;
-    for (int i = threadIdx.x; i < I; i += blockDim.x) mx = fmaxf(mx, fabsf(adt_bits_to_float(src[i], adt)));
-    mx = block_max128(mx, red);
-    float scl, inv;
-    prescale_of(mx, scl, inv);
-    uint16_t* dst = h16 + static_cast<size_t>(p) * I;
-    for (int i = threadIdx.x; i < I; i += blockDim.x)
-        dst[i] = __half_as_ushort(__float2half_rn(__fmul_rn(adt_bits_to_float(src[i], adt), scl)));
+    const float inv = row_to_f16(h + static_cast<size_t>(p) * I, h16 + static_cast<size_t>(p) * I, I, adt, red);
     if (threadIdx.x == 0) inv_out[p] = inv;
 }
 
