@@ -124,6 +124,24 @@ def dist_setup(args):
     return ws, rank, local
 
 
+def slowest_rank_ms(ms, ws, device):
+    """Every rank passes its own time per step; returns the largest over the ranks (the job's
+    time per step).  With one rank, the rank's own time."""
+    if ws == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_tokens_per_s(ws, T, ms_max):
+    """Whole-job throughput: each of the ws ranks runs T tokens per step, and a step of the job
+    takes the slowest rank's time."""
+    return ws * T / (ms_max * 1e-3)
+
+
 def captured_traffic(kernel, workload):
     """DRAM bytes (read + write) per launch of `kernel` on `workload` from a committed ncu summary
     under profiles/, or None.  A summary records its number on a line
@@ -359,11 +377,8 @@ def main():
     if ws > 1:
         torch.distributed.barrier()
     ms = statistics.median(reps)
-    ms_t = torch.tensor([ms], device="cuda")
-    if ws > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = ms_t.item()
-    value = ws * T / (ms_max * 1e-3)
+    ms_max = slowest_rank_ms(ms, ws, "cuda")
+    value = job_tokens_per_s(ws, T, ms_max)
 
     # ---- per-phase breakdown: graphs carrying event-record nodes after every launch ----------------
     # event order in a step: 6 router, 0 route list, 1 phase 1, [2 shared phase 1], 3 phase 2,

@@ -183,8 +183,10 @@ ts_status ts_moe_build_routes(const int32_t* idx, int32_t T, int32_t E, int32_t 
 /* Steps 3-5: experts + combine.                                                               */
 /* ------------------------------------------------------------------------------------------ */
 
-/* Workspace bytes ts_moe_forward needs for T tokens, k routes per token, these experts and
- * (optional, may be NULL) shared expert.  Returns 0 for invalid arguments.               */
+/* Workspace bytes ts_moe_forward needs for up to T tokens, k routes per token, these experts
+ * and (optional, may be NULL) shared expert: a workspace of this size serves every call with
+ * T or fewer tokens (a small batch can need more than a larger one, since decode-sized calls
+ * keep split-K partials).  Returns 0 for invalid arguments.                               */
 size_t ts_moe_workspace_size(int32_t T, int32_t k, const ts_moe_experts* ex,
                              const ts_moe_experts* shared);
 

@@ -3,12 +3,14 @@
 // a request the kernels cannot serve is refused with a message, never degraded (the pages'
 // convention: the Gemma-4 batched routed prefill returns Unsupported rather than quietly
 // looping the per-token kernels).
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <string>
 
 #include "../../include/ts_moe.h"
+
 #include "internal.h"
 
 using namespace tsmoe;
@@ -275,7 +277,12 @@ size_t ts_moe_workspace_size(int32_t T, int32_t k, const ts_moe_experts* ex,
                              const ts_moe_experts* shared) {
     if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->H <= 0 || ex->I <= 0) return 0;
     if (shared && (shared->I <= 0)) return 0;
-    return ws_layout(T, k, ex, shared).total;
+    // Decode-sized calls (T*k <= 64) also carry split-K partials, so a smaller batch can need
+    // more than a larger one: the size returned serves every call with up to T tokens.
+    size_t need = ws_layout(T, k, ex, shared).total;
+    const int tsplit = 64 / k;
+    if (T > tsplit && tsplit > 0) need = std::max(need, ws_layout(tsplit, k, ex, shared).total);
+    return need;
 }
 
 ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,

@@ -46,6 +46,14 @@ def test_workspace_size_grows_with_tokens(L):
     assert L.ts_moe_workspace_size(8, 0, ctypes.byref(ex), None) == 0
 
 
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_workspace_for_T_tokens_serves_every_smaller_batch(L, k):
+    # decode-sized calls (T*k <= 64) keep split-K partials, so the size must not drop past them
+    ex = _experts()
+    sizes = [L.ts_moe_workspace_size(T, k, ctypes.byref(ex), None) for T in range(1, 130)]
+    assert all(0 < a <= b for a, b in zip(sizes, sizes[1:]))
+
+
 @pytest.mark.parametrize("case,status", [
     (dict(E=300), 2), (dict(H=100), 2), (dict(fmt=7), 1), (dict(act=9), 1), (dict(ptr=0x1001), 1),
 ])

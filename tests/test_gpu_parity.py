@@ -48,6 +48,7 @@ SMALL = [
     (4, 3, dict(H=128, I=64, E=4, k=1, shared_I=64)),
     (5, 9, dict(H=256, I=512, E=8, k=2)),
     (5, 8, dict(H=4096, I=14336, E=8, k=2)),             # Mixtral-8x7B decode, 8 tokens
+    (2, 8, dict(H=256, I=128, E=256, k=8)),              # the largest expert count (256)
 ]
 
 
@@ -109,6 +110,21 @@ def _sample_tokens(T, n=6):
 
 @pytest.mark.parametrize("case", SMALL, ids=_ids)
 def test_forward_parity(case):
+    _forward_parity(case, "auto")
+
+
+# The GEMV path on both sides of the T*k = 512 boundary: at or below it the route list is built
+# inside the GEMV launches and the combine is fused into phase 2; above it the route-list
+# kernel and the separate combine run.
+@pytest.mark.parametrize("case", [(2, 64, dict(H=256, I=128, E=16, k=8)),
+                                  (2, 65, dict(H=256, I=128, E=16, k=8)),
+                                  (5, 256, dict(H=128, I=256, E=8, k=2)),
+                                  (5, 257, dict(H=128, I=256, E=8, k=2))], ids=_ids)
+def test_gemv_path_on_both_sides_of_the_fused_route_list(case):
+    _forward_parity(case, "gemv")
+
+
+def _forward_parity(case, path):
     moe = _moe()
     cfg, T, shapes = case
     L, D = _make(cfg, T, shapes)
@@ -120,7 +136,7 @@ def test_forward_parity(case):
     xg = torch.from_numpy(xin.view(np.int16)).cuda().view(synth.ADT_TORCH[c["adt"]])
     ws = moe.alloc_workspace(T, c["k"], ex, sh)
     y, y32 = moe.forward(xg, ex, torch.from_numpy(oidx).cuda(), torch.from_numpy(ow).cuda(),
-                         shared=sh, want_f32=True, ws=ws)
+                         shared=sh, want_f32=True, ws=ws, path=path)
     torch.cuda.synchronize()
     oex, osh = oracle_layer(L)
     toks = _sample_tokens(T)
@@ -198,6 +214,36 @@ def test_expert_ids_out_of_range_are_reported_and_stay_in_bounds(path, T):
     assert np.array_equal(perm[:good.size], order)
     assert np.all(perm[good.size:] == 0)
     assert np.array_equal(inv[order], np.arange(good.size))
+
+
+def test_workspace_reused_across_decode_and_prefill_calls():
+    """One workspace serves calls of different sizes and paths in a row (the in-kernel route
+    list and fused-combine counters of a decode call, the route-list kernel and tensor-core path
+    of a prefill call); a decode call after a prefill call gives the same bits as before it."""
+    moe = _moe()
+    shapes = dict(H=512, I=384, E=8, k=4)
+    Ld, Dd = _make(2, 8, shapes)
+    Lp, Dp = _make(2, 64, shapes)
+    c = Ld["cfg"]
+    ex, sh = gpu_layer(Dd)
+    ws = moe.alloc_workspace(64, c["k"], ex, sh)
+
+    def call(D, path):
+        idx, w, _, _ = moe.router_route(D["x"], D["Wr"], c["k"], mode=c["mode"],
+                                        router_bias=D["router_bias"])
+        return moe.forward(D["x"], ex, idx, w, want_f32=True, ws=ws, path=path)
+
+    y1, y1f = (t.clone() for t in call(Dd, "auto"))
+    yp, _ = call(Dp, "gemm")
+    y2, y2f = call(Dd, "auto")
+    yq, _ = call(Dp, "gemv")
+    y3, y3f = call(Dd, "auto")
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
+    for y, yf in ((y2, y2f), (y3, y3f)):
+        assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
+        assert torch.equal(yf.view(torch.int32), y1f.view(torch.int32))
+    assert torch.isfinite(yp.float()).all() and torch.isfinite(yq.float()).all()
 
 
 def test_forward_empty_batch_launches_nothing():
