@@ -668,12 +668,9 @@ int gemv_pick_tg(int K) { return make_plan(FMT_F16, K, 8).tg; }
 size_t gemv_smem_bytes(int fmt, int K, int tg) { return make_plan(fmt, K, tg).smem; }
 
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
-    // INT4 weights: the warp-independent kernel of gemv_sk.cu (measured faster there; for MXFP4
-    // at the gpt-oss shapes this kernel with its two reducer warps is still ahead)
-    if (a.fmt == FMT_INT4 && gemv_sk_fits(a.fmt, a.K, a.T)) return launch_gemv_sk(a, num_sms, s);
     KParams P;
     P.a = a;
-    const int tmax = a.dense ? a.T : a.T;   // tokens per expert never exceed T
+    const int tmax = a.T;                   // tokens per expert never exceed T
     P.p = make_plan(a.fmt, a.K, tmax < 8 ? (tmax > 0 ? tmax : 1) : 8);
     if (P.p.tg < 1) return cudaErrorInvalidValue;
     P.a.tg = P.p.tg;

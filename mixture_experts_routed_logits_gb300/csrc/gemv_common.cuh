@@ -1,6 +1,5 @@
-// gemv_common.cuh -- device helpers shared by the two decode GEMV kernels (gemv.cu: the
-// 16-bit-weight kernel with a producer warp and reducer warps; gemv_sk.cu: the packed-weight
-// kernel in which every warp streams its own range of chunks).
+// gemv_common.cuh -- device helpers of the decode GEMV (gemv.cu): the activation functions,
+// activation-row staging, the in-kernel route list and the fused combine's tile helpers.
 #pragma once
 
 #include "common.cuh"

@@ -78,8 +78,6 @@ struct GemvArgs {
     float* y_f32;                 // combine: [T][H] or nullptr
 };
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_gemv_sk(const GemvArgs& a, int num_sms, cudaStream_t s);   // INT4
-bool gemv_sk_fits(int fmt, int K, int T);
 size_t gemv_smem_bytes(int fmt, int K, int tg);
 int gemv_pick_tg(int K);
 
