@@ -182,35 +182,67 @@ router_kernel(RouteArgs a, RouterPlan p) {
         };
         if (threadIdx.x == 0)
             for (int st = 0; st < min(p.ns, nst); ++st) issue(st);
-        // token rows -> f32 in shared memory (16-byte loads, all issued before use)
-        for (int q = 0; q < ntok; ++q) {
-            const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t0 + q) * H;
-            float* xq = xs + static_cast<size_t>(q) * H;
-            if ((H & 7) == 0 && (reinterpret_cast<uintptr_t>(xr) & 15) == 0) {
-                constexpr int kMaxV = 8;
-                const int nv = H / 8;
-                uint4 v[kMaxV];
+        // token rows -> f32 in shared memory (16-byte loads, all issued before use: for a
+        // multi-token tile every token's at once, rows of up to 2 x 8 x blockDim elements;
+        // otherwise token by token)
+        const bool vec_ok = (H & 7) == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
+        if (ntok > 1 && vec_ok && H / 8 <= 2 * static_cast<int>(blockDim.x)) {
+            const int nv = H / 8;
+            uint4 v[kRouterTT][2];
 #pragma unroll
-                for (int i8 = 0; i8 < kMaxV; ++i8) {
-                    const int i = threadIdx.x + i8 * blockDim.x;
-                    if (i < nv) v[i8] = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+            for (int q = 0; q < kRouterTT; ++q)
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int i = threadIdx.x + m * blockDim.x;
+                    if (q < ntok && i < nv)
+                        v[q][m] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) +
+                                                                        static_cast<size_t>(t0 + q) * H) + i);
                 }
 #pragma unroll
-                for (int i8 = 0; i8 < kMaxV; ++i8) {
-                    const int i = threadIdx.x + i8 * blockDim.x;
-                    if (i < nv) {
-                        const uint32_t w4[4] = {v[i8].x, v[i8].y, v[i8].z, v[i8].w};
+            for (int q = 0; q < kRouterTT; ++q)
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int i = threadIdx.x + m * blockDim.x;
+                    if (q < ntok && i < nv) {
+                        float* xq = xs + static_cast<size_t>(q) * H + 8 * i;
+                        const uint32_t w4[4] = {v[q][m].x, v[q][m].y, v[q][m].z, v[q][m].w};
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
-                            xq[8 * i + 2 * h] = adt_bits_to_float(static_cast<uint16_t>(w4[h] & 0xFFFF), a.adt);
-                            xq[8 * i + 2 * h + 1] = adt_bits_to_float(static_cast<uint16_t>(w4[h] >> 16), a.adt);
+                            xq[2 * h] = adt_bits_to_float(static_cast<uint16_t>(w4[h] & 0xFFFF), a.adt);
+                            xq[2 * h + 1] = adt_bits_to_float(static_cast<uint16_t>(w4[h] >> 16), a.adt);
                         }
                     }
                 }
-                for (int j = kMaxV * blockDim.x * 8 + threadIdx.x; j < H; j += blockDim.x)
-                    xq[j] = adt_bits_to_float(xr[j], a.adt);
-            } else {
-                for (int j = threadIdx.x; j < H; j += blockDim.x) xq[j] = adt_bits_to_float(xr[j], a.adt);
+        } else {
+            for (int q = 0; q < ntok; ++q) {
+                const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t0 + q) * H;
+                float* xq = xs + static_cast<size_t>(q) * H;
+                if ((H & 7) == 0 && (reinterpret_cast<uintptr_t>(xr) & 15) == 0) {
+                    constexpr int kMaxV = 8;
+                    const int nv = H / 8;
+                    uint4 v[kMaxV];
+    #pragma unroll
+                    for (int i8 = 0; i8 < kMaxV; ++i8) {
+                        const int i = threadIdx.x + i8 * blockDim.x;
+                        if (i < nv) v[i8] = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+                    }
+    #pragma unroll
+                    for (int i8 = 0; i8 < kMaxV; ++i8) {
+                        const int i = threadIdx.x + i8 * blockDim.x;
+                        if (i < nv) {
+                            const uint32_t w4[4] = {v[i8].x, v[i8].y, v[i8].z, v[i8].w};
+    #pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                xq[8 * i + 2 * h] = adt_bits_to_float(static_cast<uint16_t>(w4[h] & 0xFFFF), a.adt);
+                                xq[8 * i + 2 * h + 1] = adt_bits_to_float(static_cast<uint16_t>(w4[h] >> 16), a.adt);
+                            }
+                        }
+                    }
+                    for (int j = kMaxV * blockDim.x * 8 + threadIdx.x; j < H; j += blockDim.x)
+                        xq[j] = adt_bits_to_float(xr[j], a.adt);
+                } else {
+                    for (int j = threadIdx.x; j < H; j += blockDim.x) xq[j] = adt_bits_to_float(xr[j], a.adt);
+                }
             }
         }
         __syncthreads();
