@@ -110,7 +110,7 @@ struct Carve {
     int* touched;     // [256]
     int* cnt;         // [256]
     int* goff;        // [257]
-    int* misc;        // [8]: 0 = ntouched, 1 = abort flag, 2 = combine on, 3 = tiles this round
+    int* misc;        // [8]: 0 = ntouched, 1 = abort flag, 2 = combine on, 3 = tiles listed now
     float* rinv;      // [2][8]: prescale inverses travelling with the partials
     uint64_t* rfull;  // [2]: partials of a unit written (16 compute warps arrive)
     uint64_t* rempty; // [2]: partial buffer read by the reducer

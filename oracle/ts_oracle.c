@@ -20,7 +20,13 @@
  *       (= router rank) order, residual = zeros or shared expert
  *                                                  [gptoss/moe.rs] module header "slot order is the ROUTER'S RANKING",
  *                                                  "zero_hidden is the residual input"
- * Readings where the pages are silent are listed in the design doc (oracle readings).
+ * Where the pages are silent this file takes these readings: top-k ties go to the lower
+ * expert id; a logit is lane l's fmaf chain over x[l+32j]*W[e][l+32j] followed by an xor
+ * butterfly (16, 8, 4, 2, 1), plus the bias as one more f32 add; the softmax runs over the k
+ * selected only; routing weights stay f32; per_expert_scale multiplies the weight, not the
+ * selection; the clamped SwiGLU adds the biases before the clamp; h is rounded to the
+ * activation type before the down projection, e stays f32, and the combine is f32 in slot
+ * order.
  */
 #include "ts_oracle.h"
 
