@@ -246,6 +246,42 @@ def test_workspace_reused_across_decode_and_prefill_calls():
     assert torch.isfinite(yp.float()).all() and torch.isfinite(yq.float()).all()
 
 
+def test_sigmoid_biased_routing_through_the_whole_layer():
+    """The biased-sigmoid mode end to end: GPU logits bit-exact, selection and weights as the
+    oracle's (wherever the selection boundary is wider than a few ulps of the two sides' expf),
+    then the whole layer on those routes against the oracle."""
+    moe = _moe()
+    L, D = _make(2, 8, dict(H=512, I=384, E=16, k=4))
+    c = dict(L["cfg"], mode="sigmoid_biased")
+    L = dict(L, cfg=c)
+    xb = bits16(L["x"])
+    _, olg, oidx, ow = oracle_route(L, xb)
+    idx, w, _, lg = moe.router_route(D["x"], D["Wr"], c["k"], mode="sigmoid_biased",
+                                     router_bias=D["router_bias"], want_logits=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(lg.cpu().numpy().view(np.uint32), olg.view(np.uint32))
+    keys = 1.0 / (1.0 + np.exp(-olg.astype(np.float64))) + L["router_bias"].cpu().numpy()
+    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+    checked = 0
+    for t in range(8):
+        srt = np.sort(keys[t])[::-1]
+        if np.min(np.abs(np.diff(srt[:c["k"] + 1]))) > 1e-6:
+            assert list(gi[t]) == list(oidx[t])
+            assert np.allclose(gw[t], ow[t], rtol=2e-6)
+            checked += 1
+    assert checked >= 6
+    ex, sh = gpu_layer(D)
+    ws = moe.alloc_workspace(8, c["k"], ex, sh)
+    y, y32 = moe.forward(D["x"], ex, idx, w, want_f32=True, ws=ws)
+    torch.cuda.synchronize()
+    oex, _ = oracle_layer(L)
+    oy, oy32, _ = oracle.moe_forward(xb, c["adt"], oex, gi, gw, nthreads=NTHREADS)
+    check_outputs(oracle.adt_bits_to_f64(bits16(y), c["adt"]), y32.double().cpu().numpy(),
+                  oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"],
+                  MAX_ABS, REL_L2)
+    assert moe.device_status(ws) == 0
+
+
 def test_forward_empty_batch_launches_nothing():
     moe = _moe()
     L, D = _make(1, 4, None)
