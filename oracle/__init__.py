@@ -81,14 +81,15 @@ def lib():
         L.or_act.argtypes = [i, ctypes.c_double, ctypes.c_double, f, f]
         L.or_act.restype = ctypes.c_double
         L.or_rmsnorm.argtypes = [vp, i, i, i, f, vp]
+        L.or_gemma_tail.argtypes = [vp, vp, vp, vp, vp, f, f, i, i, i]
         L.or_router_logits.argtypes = [vp, vp, i, i, i, i, vp]
         L.or_route.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
         L.or_build_routes.argtypes = [vp, i, i, i, vp, vp, vp]
         L.or_expert_ffn.argtypes = [ctypes.POINTER(_Experts), i, vp, i, vp, vp]
         L.or_moe_forward.argtypes = [vp, i, i, ctypes.POINTER(_Experts), vp, vp, i,
                                      ctypes.POINTER(_Experts), vp, i, vp, vp, vp, i]
-        for name in ("or_rmsnorm", "or_router_logits", "or_route", "or_build_routes",
-                     "or_expert_ffn", "or_moe_forward"):
+        for name in ("or_rmsnorm", "or_gemma_tail", "or_router_logits", "or_route",
+                     "or_build_routes", "or_expert_ffn", "or_moe_forward"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -141,6 +142,17 @@ def rmsnorm(x, adt, eps=1e-6):
     out = np.empty_like(x)
     _check(lib().or_rmsnorm(_p(x), T, H, ADT[adt], eps, _p(out)), "rmsnorm")
     return out
+
+
+def gemma_tail(y, h1, x, w_post2, w_post, adt, layer_scalar, eps=1e-6):
+    """The Gemma sandwich tail on copies of y, h1, x ([T][H] 16-bit bits): returns the new
+    (y, h1, x)."""
+    y, h1, x = _u16(y).copy(), _u16(h1).copy(), _u16(x).copy()
+    w_post2, w_post = _u16(w_post2), _u16(w_post)
+    T, H = y.shape
+    _check(lib().or_gemma_tail(_p(y), _p(h1), _p(x), _p(w_post2), _p(w_post), layer_scalar, eps,
+                               T, H, ADT[adt]), "gemma_tail")
+    return y, h1, x
 
 
 def router_logits(x, Wr, adt):

@@ -195,6 +195,58 @@ int or_rmsnorm(const uint16_t* x, int T, int H, int adt, float eps, uint16_t* xn
     return 0;
 }
 
+/* Weighted RMSNorm of one row: out_j = adt((v_j * r) * w_j), r = 1/sqrt(mean(v^2) + eps) with
+ * the fixed-order sum above, w bf16, every step one rounded f32 op. */
+static void rms_weighted(const float* v, const uint16_t* w, int H, float eps, int adt, uint16_t* out) {
+    float ss = or_dot32f(v, v, H);
+    float ms = ss / (float)H;
+    float r = 1.0f / sqrtf(ms + eps);
+    for (int j = 0; j < H; ++j) {
+        float a = v[j] * r;
+        float b = a * (float)or_bf16_to_double(w[j]);
+        out[j] = double_to_adt((double)b, adt);
+    }
+}
+
+/* The Gemma sandwich tail that follows the routed phase 2 ([gemma4/moe_batch] routed prefill,
+ * per token, in place on 16-bit buffers):
+ *   y  <- rms_w(y, w_post2)            post_feedforward_layernorm_2
+ *   h1 <- adt(h1 + y)                  the dense branch plus the normalised routed output
+ *   f   = rms_w(h1, w_post)            post_feedforward_layernorm
+ *   x  <- adt(x + f)                   the residual stream
+ *   x  <- adt(x * layer_scalar)
+ * The weight multiply reads plainly as v * r * w (the pages name the kernel "rms_norm_bf16w"
+ * without its body). */
+int or_gemma_tail(uint16_t* y, uint16_t* h1, uint16_t* x, const uint16_t* w_post2,
+                  const uint16_t* w_post, float layer_scalar, float eps, int T, int H, int adt) {
+    if (H % 32) return -1;
+    float* v = (float*)malloc(sizeof(float) * H);
+    uint16_t* f = (uint16_t*)malloc(sizeof(uint16_t) * H);
+    if (!v || !f) { free(v); free(f); return -2; }
+    for (int t = 0; t < T; ++t) {
+        uint16_t* yt = y + (size_t)t * H;
+        uint16_t* ht = h1 + (size_t)t * H;
+        uint16_t* xt = x + (size_t)t * H;
+        for (int j = 0; j < H; ++j) v[j] = (float)adt_to_double(yt[j], adt);
+        rms_weighted(v, w_post2, H, eps, adt, yt);
+        for (int j = 0; j < H; ++j) {
+            float s = (float)adt_to_double(ht[j], adt) + (float)adt_to_double(yt[j], adt);
+            ht[j] = double_to_adt((double)s, adt);
+            v[j] = (float)adt_to_double(ht[j], adt);
+        }
+        rms_weighted(v, w_post, H, eps, adt, f);
+        for (int j = 0; j < H; ++j) {
+            float s = (float)adt_to_double(xt[j], adt) + (float)adt_to_double(f[j], adt);
+            uint16_t xs = double_to_adt((double)s, adt);
+            float m = (float)adt_to_double(xs, adt) * layer_scalar;
+            xt[j] = double_to_adt((double)m, adt);
+        }
+    }
+    free(v);
+    free(f);
+    return 0;
+}
+
 /* a1: raw router logits (no bias), r[t][e] = sum_h x[t][h] * W_r[e][h] in the fixed order. */
 int or_router_logits(const uint16_t* x, const uint16_t* Wr, int T, int H, int E, int adt,
                      float* logits) {

@@ -57,6 +57,8 @@ float or_dot32f(const float* a, const float* b, int n);
 double or_act(int act, double g, double u, float limit, float alpha);
 
 int or_rmsnorm(const uint16_t* x, int T, int H, int adt, float eps, uint16_t* xn);
+int or_gemma_tail(uint16_t* y, uint16_t* h1, uint16_t* x, const uint16_t* w_post2,
+                  const uint16_t* w_post, float layer_scalar, float eps, int T, int H, int adt);
 int or_router_logits(const uint16_t* x, const uint16_t* Wr, int T, int H, int E, int adt,
                      float* logits);
 int or_route(const float* logits, const float* bias, const float* scale, int T, int E, int k,

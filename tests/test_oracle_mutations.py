@@ -24,6 +24,10 @@ MUTATIONS = {
                               "for (int r = n - 1; r >= 0; --r)\n            if (idx[r] == e)"),
     "h not rounded to 16 bits": ("h_out[i] = adt_to_double(double_to_adt(h, adt), adt);",
                                  "h_out[i] = h;"),
+    "tail drops the layer scalar": ("float m = (float)adt_to_double(xs, adt) * layer_scalar;",
+                                    "float m = (float)adt_to_double(xs, adt);"),
+    "tail skips the dense branch": ("float s = (float)adt_to_double(ht[j], adt) + (float)adt_to_double(yt[j], adt);",
+                                    "float s = (float)adt_to_double(yt[j], adt);"),
 }
 
 

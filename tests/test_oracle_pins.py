@@ -413,3 +413,69 @@ def test_hand_example_closed_form():
     h = float(np.float16(float(2 / (1 + mpmath.exp(-1)))))   # 1.462117... -> f16 1.4619140625
     assert h == 1.4619140625
     assert np.all(yf[0] == np.float32(h))
+
+
+# ---------------------------------------------------------------- Gemma sandwich tail
+# ([gemma4/moe_batch] routed prefill: rms-norm the routed output with
+# post_feedforward_layernorm_2, add it to the dense branch h1, rms-norm that with
+# post_feedforward_layernorm, add it to the residual x, multiply x by the layer scalar)
+
+def _adt_bits(a, adt):
+    t = torch.from_numpy(np.asarray(a, np.float32))
+    t = t.to(torch.bfloat16 if adt == "bf16" else torch.float16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _tail_inputs(adt, T=3, H=256, seed=0):
+    rng = np.random.default_rng(seed)
+    y = _adt_bits(rng.standard_normal((T, H)) * 3.0, adt)
+    h1 = _adt_bits(rng.standard_normal((T, H)), adt)
+    x = _adt_bits(rng.standard_normal((T, H)) * 2.0, adt)
+    w2 = _adt_bits(1.0 + 0.1 * rng.standard_normal(H), "bf16")
+    w1 = _adt_bits(1.0 + 0.1 * rng.standard_normal(H), "bf16")
+    return y, h1, x, w2, w1
+
+
+@pytest.mark.parametrize("adt", ["bf16", "f16"])
+def test_tail_with_unit_weights_is_two_plain_rmsnorms(adt):
+    # w = 1, h1 = x = 0, scalar 1: y' = h1' = rms(y) and x' = rms(rms(y)), bit for bit, against
+    # the separately pinned unweighted RMSNorm
+    y = _tail_inputs(adt)[0]
+    zero = np.zeros_like(y)
+    one = _adt_bits(np.ones(y.shape[1]), "bf16")
+    yo, ho, xo = oracle.gemma_tail(y, zero, zero, one, one, adt, 1.0)
+    r1 = oracle.rmsnorm(y, adt)
+    assert np.array_equal(yo, r1)
+    assert np.array_equal(ho, r1)
+    assert np.array_equal(xo, oracle.rmsnorm(r1, adt))
+
+
+@pytest.mark.parametrize("adt", ["bf16", "f16"])
+def test_tail_power_of_two_weight_and_scalar_scale_exactly(adt):
+    y, h1, x, w2, w1 = _tail_inputs(adt, seed=1)
+    H = y.shape[1]
+    one = _adt_bits(np.ones(H), "bf16")
+    two = _adt_bits(np.full(H, 2.0), "bf16")
+    base = oracle.gemma_tail(y, h1, x, w2, w1, adt, 1.0)
+    x4 = oracle.gemma_tail(y, h1, x, w2, w1, adt, 4.0)[2]
+    assert np.array_equal(oracle.adt_bits_to_f64(x4, adt), 4.0 * oracle.adt_bits_to_f64(base[2], adt))
+    y_one = oracle.gemma_tail(y, h1, x, one, w1, adt, 1.0)[0]
+    y_two = oracle.gemma_tail(y, h1, x, two, w1, adt, 1.0)[0]
+    assert np.array_equal(oracle.adt_bits_to_f64(y_two, adt), 2.0 * oracle.adt_bits_to_f64(y_one, adt))
+
+
+@pytest.mark.parametrize("adt", ["bf16", "f16"])
+def test_tail_with_zero_routed_output_normalises_the_dense_branch(adt):
+    _, h1, x, w2, w1 = _tail_inputs(adt, seed=2)
+    zero = np.zeros_like(h1)
+    s = 0.75
+    yo, ho, xo = oracle.gemma_tail(zero, h1, x, w2, w1, adt, s)
+    assert not np.any(oracle.adt_bits_to_f64(yo, adt))
+    assert np.array_equal(ho, h1)
+    hd, xd = oracle.adt_bits_to_f64(h1, adt), oracle.adt_bits_to_f64(x, adt)
+    wd = oracle.bf16_bits_to_f64(w1)
+    f = hd / np.sqrt(np.mean(hd * hd, axis=1, keepdims=True) + 1e-6) * wd
+    want = (xd + f) * s
+    u = 2.0 ** (-7 if adt == "bf16" else -10)          # one unit in the last place, relative
+    bound = (s * (np.abs(f) + np.abs(xd + f)) + np.abs(want)) * u + 1e-30
+    assert np.all(np.abs(oracle.adt_bits_to_f64(xo, adt) - want) <= bound)
