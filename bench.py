@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"],
                    help="expert path passed to ts_moe_forward_path")
+    p.add_argument("--gemma-tail", action="store_true",
+                   help="append the Gemma sandwich tail (ts_moe_gemma_tail) to every step")
     p.add_argument("--profile", action="store_true",
                    help="short run for profiler captures: one timed repetition, few samples")
     return p.parse_args()
@@ -296,6 +298,14 @@ def main():
                     w=torch.empty((T, k), dtype=torch.float32, device="cuda"),
                     xn=torch.empty_like(L["x"]) if cfg["rmsnorm"] else None,
                     y=torch.empty_like(L["x"]))
+        if args.gemma_tail:
+            # the tail's other inputs: the dense branch h1, the residual stream, the two
+            # post-FFN norm weights (around 1) and the layer scalar
+            g = torch.Generator(device="cuda").manual_seed(li)
+            outs.update(h1=torch.randn(L["x"].shape, generator=g, device="cuda").to(L["x"].dtype),
+                        xres=torch.randn(L["x"].shape, generator=g, device="cuda").to(L["x"].dtype),
+                        w_post2=(1 + 0.1 * torch.randn(H, generator=g, device="cuda")).to(torch.bfloat16),
+                        w_post=(1 + 0.1 * torch.randn(H, generator=g, device="cuda")).to(torch.bfloat16))
         layers.append(dict(L=L, ex=ex, sh=sh, ws=wsb, **outs))
     torch.cuda.synchronize()
 
@@ -307,9 +317,12 @@ def main():
         xin = ly["xn"] if cfg["rmsnorm"] else L["x"]
         moe.forward(xin, ly["ex"], ly["idx"], ly["w"], shared=ly["sh"], ws=ly["ws"],
                     out=(ly["y"], None), path=args.path, stream=stream)
+        if args.gemma_tail:
+            moe.gemma_tail(ly["y"], ly["h1"], ly["xres"], ly["w_post2"], ly["w_post"], 0.5,
+                           stream=stream)
 
     # ---- CUDA graphs: one per layer, plus a copy with per-phase events -------------------------------
-    nph = 7
+    nph = 8
     phase_ev = [torch.cuda.Event(enable_timing=True) for _ in range(nph)]
     for ev in phase_ev:      # the library records them inside the graphs; torch only lets
         ev.record()          # elapsed_time() read events it has seen recorded once
@@ -342,7 +355,7 @@ def main():
     fused_decode = (not gemm_path) and T * k <= 512
     n_launch_step = ((3 if fused_decode else 5 + (1 if gemm_path else 0)
                       + (1 if gemm_path and cfg["fmt"] == "mxfp4" else 0))
-                     + (2 if cfg.get("shared_I") else 0))
+                     + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail else 0))
 
     def timed(K):
         b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -382,11 +395,13 @@ def main():
 
     # ---- per-phase breakdown: graphs carrying event-record nodes after every launch ----------------
     # event order in a step: 6 router, 0 route list, 1 phase 1, [2 shared phase 1], 3 phase 2,
-    # [4 shared phase 2], 5 combine
+    # [4 shared phase 2], 5 combine, [7 Gemma sandwich tail]
     if gemm_path:
         order = [6, 0, 1, 3, 5]
     else:   # GEMV: routed phase 1, shared phase 1, shared phase 2, routed phase 2 (+ combine)
         order = [6, 0, 1] + ([2, 4] if cfg.get("shared_I") else []) + [3, 5]
+    if args.gemma_tail:
+        order = order + [7]
     samples = {moe.PHASES[j]: [] for j in order}
     for i in range(3 if args.profile else min(args.steps, 50)):
         flush.zero_()
@@ -487,7 +502,8 @@ def main():
                          f"{n_layers} rotating weight sets",
                    "timing": "CUDA graph per step, CUDA events per step; the K-step loop repeated "
                              f"{len(reps)}x under clock sampling, median repetition",
-                   "touched_experts": int(n_touched), "parallelism": f"replicas x{ws}"},
+                   "touched_experts": int(n_touched), "parallelism": f"replicas x{ws}",
+                   "gemma_tail": bool(args.gemma_tail)},
         "roofline": roof,
         "step_tflops": None if step_tf is None else {"TFLOPs": step_tf, "frac": step_tf / bf16_sust},
         "step_hbm": {"bytes": step_bytes, "GBps": step_bytes / (ms_max * 1e-3) / 1e9,

@@ -237,6 +237,27 @@ ts_status ts_moe_forward_noalloc(const void* x, int32_t adt, int32_t T, const ts
                                  void* stream);
 
 /* ------------------------------------------------------------------------------------------ */
+/* After step 5 (Gemma layers): the sandwich tail.                                             */
+/* ------------------------------------------------------------------------------------------ */
+
+/* The per-token tail that the Gemma-4 batched routed prefill (src/families/gemma4/moe_batch.rs)
+ * encodes after the fused phase 2, in place on three 16-bit [T][H] buffers:
+ *   y  <- adt(rms(y)  * w_post2)   rms(v) = v * (1 / sqrt(mean(v^2) + eps)), w bf16
+ *   h1 <- adt(h1 + y)              the dense branch plus the normalised routed output
+ *   f   = adt(rms(h1) * w_post)
+ *   x  <- adt(adt(x + f) * layer_scalar)
+ * Every step is one rounded f32 op (the weight multiply reads as (v * r) * w); the sum of
+ * squares takes the fixed order of ts_moe_router_route's RMSNorm, so the result is bit-exact.
+ *   y, h1, x          device adt [T][H], read and written (three distinct buffers)
+ *   w_post2, w_post   device bf16 [H]
+ *   adt               TS_DT_F16 or TS_DT_BF16
+ * H must be a multiple of 32 and at most 8192 (TS_ERR_UNSUPPORTED otherwise).  T == 0 launches
+ * nothing.                                                                                  */
+ts_status ts_moe_gemma_tail(void* y, void* h1, void* x, const void* w_post2, const void* w_post,
+                            float layer_scalar, float eps, int32_t adt, int32_t T, int32_t H,
+                            void* stream);
+
+/* ------------------------------------------------------------------------------------------ */
 /* Diagnostics.                                                                                */
 /* ------------------------------------------------------------------------------------------ */
 
@@ -254,7 +275,8 @@ ts_status ts_moe_device_status(void* ws, int32_t* code, void* stream);
  * stream right after launching phase i, for the phases that exist:
  *   0 route list, 1 expert phase 1 (gate/up + activation), 2 shared-expert phase 1,
  *   3 expert phase 2 (down), 4 shared-expert phase 2, 5 combine;
- * and ts_moe_route / ts_moe_router_route record events[6] after the router kernel.
+ * ts_moe_route / ts_moe_router_route record events[6] after the router kernel and
+ * ts_moe_gemma_tail records events[7] after the tail.
  * On a capturing stream the events become graph event-record nodes, so graph replays record
  * them too.  The caller owns the events.                                                     */
 ts_status ts_moe_set_phase_events(void* const* events, int32_t n);

@@ -75,6 +75,7 @@ def lib():
             "ts_moe_forward_noalloc": ([vp, i32, i32, pe, vp, vp, i32, pe, vp, vp, vp],
                                        ctypes.c_int),
             "ts_moe_set_phase_events": ([ctypes.POINTER(vp), i32], ctypes.c_int),
+            "ts_moe_gemma_tail": ([vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -188,6 +189,17 @@ def router_route(x, W_r, k, mode="softmax_k", router_bias=None, per_expert_scale
     return idx, w, xn, logits
 
 
+def gemma_tail(y, h1, x, w_post2, w_post, layer_scalar, eps=1e-6, stream=None):
+    """The Gemma sandwich tail in place on y, h1, x ([T,H] f16/bf16): y <- rms(y) * w_post2,
+    h1 <- h1 + y, x <- (x + rms(h1) * w_post) * layer_scalar (ts_moe_gemma_tail)."""
+    import torch
+    T, H = y.shape
+    adt = {torch.float16: "f16", torch.bfloat16: "bf16"}[y.dtype]
+    check(lib().ts_moe_gemma_tail(_ptr(y), _ptr(h1), _ptr(x), _ptr(w_post2), _ptr(w_post),
+                                  float(layer_scalar), float(eps), ADT[adt], T, H, _stream(stream)))
+    return y, h1, x
+
+
 def build_routes(idx, E, stream=None):
     import torch
     T, k = idx.shape
@@ -256,7 +268,7 @@ def forward_noalloc(x, ex: Experts, idx, w, shared: Experts | None = None, want_
 
 
 PHASES = ("route_list", "experts_phase1", "shared_phase1", "experts_phase2", "shared_phase2",
-          "combine", "router")
+          "combine", "router", "gemma_tail")
 
 
 def set_phase_events(events):

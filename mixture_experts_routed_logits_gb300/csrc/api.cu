@@ -532,6 +532,37 @@ ts_status ts_moe_set_phase_events(void* const* events, int32_t n) {
     return TS_OK;
 }
 
+ts_status ts_moe_gemma_tail(void* y, void* h1, void* x, const void* w_post2, const void* w_post,
+                            float layer_scalar, float eps, int32_t adt, int32_t T, int32_t H,
+                            void* stream) {
+    g_err.clear();
+    const char* what = "ts_moe_gemma_tail";
+    if (adt != TS_DT_F16 && adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, adt);
+    if (T < 0 || H <= 0) return fail(TS_ERR_INVALID_ARG, "%s: bad T=%d / H=%d", what, T, H);
+    if (H % 32 || H > kTailMaxH)
+        return fail(TS_ERR_UNSUPPORTED, "%s: H=%d must be a multiple of 32 and at most %d", what, H, kTailMaxH);
+    if (T == 0) return TS_OK;
+    if (!y || !h1 || !x || !w_post2 || !w_post) return fail(TS_ERR_INVALID_ARG, "%s: NULL pointer", what);
+    if (y == h1 || y == x || h1 == x) return fail(TS_ERR_INVALID_ARG, "%s: y, h1 and x must be distinct", what);
+    if (!aligned(y, 2) || !aligned(h1, 2) || !aligned(x, 2) || !aligned(w_post2, 2) || !aligned(w_post, 2))
+        return fail(TS_ERR_INVALID_ARG, "%s: pointers must be 2-byte aligned", what);
+    TailArgs a{};
+    a.y = static_cast<uint16_t*>(y);
+    a.h1 = static_cast<uint16_t*>(h1);
+    a.x = static_cast<uint16_t*>(x);
+    a.w_post2 = static_cast<const uint16_t*>(w_post2);
+    a.w_post = static_cast<const uint16_t*>(w_post);
+    a.layer_scalar = layer_scalar;
+    a.eps = eps;
+    a.adt = adt;
+    a.T = T;
+    a.H = H;
+    cudaError_t e = launch_gemma_tail(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = phase_mark(7, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return TS_OK;
+}
+
 ts_status ts_moe_device_status(void* ws, int32_t* code, void* stream) {
     g_err.clear();
     if (!ws || !code) return fail(TS_ERR_INVALID_ARG, "ts_moe_device_status: NULL pointer");

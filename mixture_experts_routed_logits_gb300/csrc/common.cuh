@@ -222,6 +222,16 @@ __device__ __forceinline__ float warp_sum_xor(float v) {
     return v;
 }
 
+// Fixed-order f32 dot product of a warp: lane l sums fmaf(a[l+32j], b[l+32j]) over j, then an
+// xor butterfly 16, 8, 4, 2, 1.  Every lane returns the same bits.
+template <typename LoadB>
+__device__ __forceinline__ float warp_dot_fixed(const float* a, LoadB loadb, int H, int lane) {
+    float p = 0.0f;
+#pragma unroll 8
+    for (int j = lane; j < H; j += 32) p = __fmaf_rn(a[j], loadb(j), p);
+    return warp_sum_xor(p);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

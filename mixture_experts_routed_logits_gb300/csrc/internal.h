@@ -91,6 +91,19 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 
+// the Gemma sandwich tail (tail.cu): in place on y, h1, x [T][H] 16-bit
+constexpr int kTailMaxH = 8192;
+struct TailArgs {
+    uint16_t* y;            // routed output -> normalised routed output
+    uint16_t* h1;           // dense branch -> h1 + normalised routed output
+    uint16_t* x;            // residual stream -> (x + normalised h1) * layer_scalar
+    const uint16_t* w_post2;   // [H] bf16 post_feedforward_layernorm_2
+    const uint16_t* w_post;    // [H] bf16 post_feedforward_layernorm
+    float layer_scalar, eps;
+    int adt, T, H;
+};
+cudaError_t launch_gemma_tail(const TailArgs& a, cudaStream_t s);
+
 // ------------------------------------------------------------------------------------------
 // tensor-core grouped GEMM (prefill) path
 // ------------------------------------------------------------------------------------------

@@ -43,16 +43,6 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
     return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
-// Fixed-order f32 dot product of a warp: lane l sums fmaf(a[l+32j], b[l+32j]) over j, then an
-// xor butterfly 16, 8, 4, 2, 1.  Every lane returns the same bits.
-template <typename LoadB>
-__device__ __forceinline__ float warp_dot_fixed(const float* a, LoadB loadb, int H, int lane) {
-    float p = 0.0f;
-#pragma unroll 8
-    for (int j = lane; j < H; j += 32) p = __fmaf_rn(a[j], loadb(j), p);
-    return warp_sum_xor(p);
-}
-
 // Router layout.  A CTA takes a tile of `tt` tokens and a group of `ec` experts; the `cl` expert
 // groups of a token tile form one thread-block cluster, so a decode batch of a few tokens still
 // spreads over many SMs.  The CTA's router rows stream through shared memory in stages of `rb`

@@ -125,3 +125,15 @@ def test_build_routes_and_pack_reject(L):
                          ctypes.c_void_p(0x101), 1 << 20, None) == 1          # misaligned
     assert L.ts_moe_pack(2, 1, 16, 32, ctypes.c_void_p(0x100), ctypes.c_void_p(0x100),
                          ctypes.c_void_p(0x100), 10, None) == 1               # too small
+
+
+def test_gemma_tail_rejects_bad_arguments(L):
+    p = [ctypes.c_void_p(0x1000 + 0x100 * i) for i in range(5)]
+    f = ctypes.c_float
+    assert L.ts_moe_gemma_tail(*p, f(1.0), f(1e-6), 0, 0, 256, None) == 0      # T == 0: nothing
+    assert L.ts_moe_gemma_tail(*p, f(1.0), f(1e-6), 5, 4, 256, None) == 1      # bad adt
+    assert L.ts_moe_gemma_tail(*p, f(1.0), f(1e-6), 1, 4, 100, None) == 2      # H % 32
+    assert L.ts_moe_gemma_tail(*p, f(1.0), f(1e-6), 1, 4, 8224, None) == 2     # H > 8192
+    assert L.ts_moe_gemma_tail(None, *p[1:], f(1.0), f(1e-6), 1, 4, 256, None) == 1
+    assert L.ts_moe_gemma_tail(p[0], p[0], *p[2:], f(1.0), f(1e-6), 1, 4, 256, None) == 1   # y == h1
+    assert b"distinct" in L.ts_last_error()

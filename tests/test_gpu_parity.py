@@ -282,6 +282,27 @@ def test_sigmoid_biased_routing_through_the_whole_layer():
     assert moe.device_status(ws) == 0
 
 
+@pytest.mark.parametrize("adt,T,H", [("bf16", 1, 256), ("bf16", 8, 2048), ("f16", 37, 2880),
+                                     ("bf16", 3, 8192)])
+def test_gemma_tail_bit_exact(adt, T, H):
+    """The Gemma sandwich tail on the GPU equals the oracle bit for bit (y, h1 and x)."""
+    moe = _moe()
+    rng = np.random.default_rng(T * 100 + H)
+    tdt = synth.ADT_TORCH[adt]
+    y = torch.from_numpy((rng.standard_normal((T, H)) * 3).astype(np.float32)).to(tdt)
+    h1 = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(tdt)
+    x = torch.from_numpy((rng.standard_normal((T, H)) * 2).astype(np.float32)).to(tdt)
+    w2 = torch.from_numpy((1 + 0.1 * rng.standard_normal(H)).astype(np.float32)).to(torch.bfloat16)
+    w1 = torch.from_numpy((1 + 0.1 * rng.standard_normal(H)).astype(np.float32)).to(torch.bfloat16)
+    oy, oh, ox = oracle.gemma_tail(bits16(y), bits16(h1), bits16(x), bits16(w2), bits16(w1), adt, 0.8)
+    gy, gh, gx = (t.cuda() for t in (y, h1, x))
+    moe.gemma_tail(gy, gh, gx, w2.cuda(), w1.cuda(), 0.8)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(gy), oy)
+    assert np.array_equal(bits16(gh), oh)
+    assert np.array_equal(bits16(gx), ox)
+
+
 def test_forward_empty_batch_launches_nothing():
     moe = _moe()
     L, D = _make(1, 4, None)
