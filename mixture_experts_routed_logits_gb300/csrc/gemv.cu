@@ -663,10 +663,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
 }  // namespace
 
-int gemv_pick_tg(int K) { return make_plan(FMT_F16, K, 8).tg; }
-
-size_t gemv_smem_bytes(int fmt, int K, int tg) { return make_plan(fmt, K, tg).smem; }
-
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
     KParams P;
     P.a = a;

@@ -78,8 +78,6 @@ struct GemvArgs {
     float* y_f32;                 // combine: [T][H] or nullptr
 };
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s);
-size_t gemv_smem_bytes(int fmt, int K, int tg);
-int gemv_pick_tg(int K);
 
 struct CombineArgs {
     const float* e;        // [T*k][H] f32 by route id
