@@ -87,7 +87,8 @@ def test_router_bit_exact(case):
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 32, 4), (8, 128, 8), (512, 32, 4), (2048, 8, 2),
-                                   (1500, 256, 16), (3, 5, 5)])
+                                   (1500, 256, 16), (3, 5, 5),
+                                   (131072, 64, 8)])          # a million routes: many chunks
 def test_build_routes_bit_exact(T, E, k):
     moe = _moe()
     rng = np.random.default_rng(T * 1000 + E)
