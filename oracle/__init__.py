@@ -88,8 +88,11 @@ def lib():
         L.or_expert_ffn.argtypes = [ctypes.POINTER(_Experts), i, vp, i, vp, vp]
         L.or_moe_forward.argtypes = [vp, i, i, ctypes.POINTER(_Experts), vp, vp, i,
                                      ctypes.POINTER(_Experts), vp, i, vp, vp, vp, i]
+        L.or_expert_pre.argtypes = [ctypes.POINTER(_Experts), i, vp, vp, vp, vp, vp]
+        L.or_act_n.argtypes = [i, vp, vp, i, f, f, vp]
+        L.or_act_n.restype = None
         for name in ("or_rmsnorm", "or_gemma_tail", "or_router_logits", "or_route",
-                     "or_build_routes", "or_expert_ffn", "or_moe_forward"):
+                     "or_build_routes", "or_expert_ffn", "or_expert_pre", "or_moe_forward"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -193,6 +196,25 @@ def expert_ffn(ex: Experts, e, xin, adt):
     _check(lib().or_expert_ffn(ctypes.byref(ex.c), e, _p(xin), ADT[adt], _p(h), _p(eo)),
            "expert_ffn")
     return h, eo
+
+
+def expert_pre(ex: Experts, e, xin):
+    """Phase-1 pre-activation sums of expert e for one input row (float64, biases added) and
+    their absolute sums: (g [I], u [I], sum |W_g x| [I], sum |W_u x| [I])."""
+    xin = np.ascontiguousarray(xin, np.float64)
+    g, u, sg, su = (np.empty(ex.I, np.float64) for _ in range(4))
+    _check(lib().or_expert_pre(ctypes.byref(ex.c), e, _p(xin), _p(g), _p(u), _p(sg), _p(su)),
+           "expert_pre")
+    return g, u, sg, su
+
+
+def act(ex: Experts, g, u):
+    """The expert set's gated activation over arrays g, u (float64)."""
+    g = np.ascontiguousarray(g, np.float64)
+    u = np.ascontiguousarray(u, np.float64)
+    out = np.empty_like(g)
+    lib().or_act_n(ex.c.act, _p(g), _p(u), g.size, ex.c.limit, ex.c.alpha, _p(out))
+    return out
 
 
 def moe_forward(x, adt, ex: Experts, idx, w, shared: Experts | None = None, tokens=None,

@@ -396,6 +396,40 @@ int or_expert_ffn(const or_experts* X, int e, const double* xin, int adt, double
     return 0;
 }
 
+/* The pre-activation sums of phase 1 for one (token, expert) pair, exposed so that the tests can
+ * bound how far any f32 evaluation of them may fall from these exact values:
+ *   g[i] = sum_c W_g[e][i][c] x[c] + b_g[e][i],   u[i] likewise with W_u, b_u   (double)
+ *   sg[i] = sum_c |W_g[e][i][c] x[c]|,             su[i] likewise              (double)
+ * The same dequantisation and double sums as or_expert_ffn; nothing is rounded. */
+int or_expert_pre(const or_experts* X, int e, const double* xin, double* g_out, double* u_out,
+                  double* sg_out, double* su_out) {
+    int H = X->H, I = X->I;
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0, sg = 0.0, su = 0.0;
+        for (int c = 0; c < H; ++c) {
+            double pg = or_weight(X, 0, e, i, c) * xin[c];
+            double pu = or_weight(X, 1, e, i, c) * xin[c];
+            g += pg;
+            u += pu;
+            sg += fabs(pg);
+            su += fabs(pu);
+        }
+        if (X->gate_b) g += or_bf16_to_double(X->gate_b[(size_t)e * I + i]);
+        if (X->up_b) u += or_bf16_to_double(X->up_b[(size_t)e * I + i]);
+        g_out[i] = g;
+        u_out[i] = u;
+        sg_out[i] = sg;
+        su_out[i] = su;
+    }
+    return 0;
+}
+
+/* or_act over n pairs (g[i], u[i]) -> out[i], in double. */
+void or_act_n(int act, const double* g, const double* u, int n, float limit, float alpha,
+              double* out) {
+    for (int i = 0; i < n; ++i) out[i] = or_act(act, g[i], u[i], limit, alpha);
+}
+
 /* a4..a7 for the tokens listed in `tokens` (all T if tokens == NULL).  Output row q of
  * y / y_f32 belongs to token tokens[q].  The combine runs in f32, slot by slot:
  * acc = seed; acc = acc + w[t][s] * e_s (a rounded multiply, then a rounded add);

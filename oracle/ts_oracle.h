@@ -67,6 +67,10 @@ int or_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off, int32
                     int32_t* inv);
 int or_expert_ffn(const or_experts* X, int e, const double* xin, int adt, double* h_out,
                   float* e_out);
+int or_expert_pre(const or_experts* X, int e, const double* xin, double* g_out, double* u_out,
+                  double* sg_out, double* su_out);
+void or_act_n(int act, const double* g, const double* u, int n, float limit, float alpha,
+              double* out);
 int or_moe_forward(const uint16_t* x, int adt, int T, const or_experts* X, const int32_t* idx,
                    const float* w, int k, const or_experts* shared, const int32_t* tokens,
                    int ntok, uint16_t* y, float* y_f32, float* e_routes, int nthreads);

@@ -119,24 +119,120 @@ def ulp16(v, adt):
     return np.ldexp(1.0, (e - (p - 1)).astype(np.int64))
 
 
+def round16(v, adt):
+    """Round float64 values to the nearest 16-bit value of the activation type (ties to even),
+    returned as float64 (numpy; finite values within the type's range)."""
+    v = np.asarray(v, np.float64)
+    q = ulp16(v, adt)
+    return np.round(v / q) * q
+
+
+# f32 evaluation error of a phase-1 pre-activation, as a multiple kappa of 2^-24 * sum |w_c x_c|
+# (the absolute sum of its products).  The products are exact on both sides (dequantised
+# weights times 16-bit activations); the GPU adds them in f32 in blocked chains, so its error is
+# a small multiple of the unit roundoff times the absolute sum.  Measured on GB300 over every
+# sampled h element of the five configurations (the smallest kappa that names each element the
+# GPU rounded differently from the oracle): at most 0.5 on the streaming GEMV path and on the
+# MXFP4 tensor-core path, at most 4 on the tensor-core path with 16-bit weights (its K = 4096
+# reduction runs through 256 chained MMA steps).  The bounds keep a margin of 4x and 2x.
+KAPPA_GEMV = 2.0
+KAPPA_TC16 = 8.0
+KAPPA = KAPPA_GEMV
+
+
+def kappa_for(cfg, T, path):
+    """kappa of the expert path a call takes (the library's automatic choice for path="auto")."""
+    tc_fmt = cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"]
+    tc_shape = cfg["H"] % 64 == 0 and cfg["I"] % 64 == 0
+    tc = tc_fmt and tc_shape and (path == "gemm" or (path == "auto" and T > 8))
+    return KAPPA_TC16 if (tc and cfg["fmt"] in ("f16", "bf16")) else KAPPA_GEMV
+# f32 evaluation of the activation itself (expf / tanhf, a divide, two multiplies), relative
+ACT_REL = 2.0 ** -20
+# non-flip f32 error of an output beside the flips (down projection and combine in f32)
+OUT_SLACK = 1e-3
+
+
+def _abs_rows(fmt, codes_e, scales_e):
+    """|W| of one expert matrix as float32 [R][K] (canonical layout)."""
+    if fmt in ("f16", "bf16"):
+        return codes_e.detach().cpu().float().abs().numpy()
+    return np.abs(np_dequant(fmt, codes_e.detach().cpu(),
+                             None if scales_e is None else scales_e.detach().cpu())).astype(np.float32)
+
+
+def flip_allowance(L, oex, osh, xin_rows_f64, idx_rows, w_rows, adt, kappa=KAPPA, nthreads=1):
+    """Per-output allowance [n, H] for the 16-bit rounding of h, from the oracle alone.
+
+    Both sides round the phase-1 output h to the 16-bit activation type before the down
+    projection.  For each h element the oracle's exact pre-activations g, u are widened by the
+    f32 evaluation error (kappa * 2^-24 * sum|products|); if the activation over that box
+    straddles a 16-bit rounding boundary, the element may round to either neighbour on the GPU.
+    Such an element moves output j of its token by at most gap * |W_d[j, i]| * w (gap = the two
+    roundings' distance); the allowance of output j is the sum over the flagged elements of
+    every route of that token (and of the shared expert, weight 1).  Elements away from a
+    boundary contribute nothing, so outputs of tokens without flagged elements keep the plain
+    bar.  Returns (allowance, number of flagged elements)."""
+    import concurrent.futures
+    c = L["cfg"]
+    H = c["H"]
+    n = len(xin_rows_f64)
+    allow = np.zeros((n, H), np.float64)
+    jobs = []                                  # (expert set, expert id, row q, weight)
+    for q in range(n):
+        for s, e in enumerate(idx_rows[q]):
+            jobs.append(("routed", int(e), q, float(w_rows[q][s])))
+        if osh is not None:
+            jobs.append(("shared", 0, q, 1.0))
+
+    def gaps(job):
+        which, e, q, _ = job
+        ex = oex if which == "routed" else osh
+        g, u, sg, su = oracle.expert_pre(ex, e, xin_rows_f64[q])
+        dg, du = kappa * 2.0 ** -24 * sg, kappa * 2.0 ** -24 * su
+        h0 = oracle.act(ex, g, u)
+        lo, hi = h0.copy(), h0.copy()
+        for a in (-1.0, 1.0):
+            for b in (-1.0, 1.0):
+                hc = oracle.act(ex, g + a * dg, u + b * du)
+                lo, hi = np.minimum(lo, hc), np.maximum(hi, hc)
+        lo -= ACT_REL * np.abs(h0)
+        hi += ACT_REL * np.abs(h0)
+        return np.abs(round16(hi, adt) - round16(lo, adt))
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, nthreads)) as pool:
+        gap_list = list(pool.map(gaps, jobs))
+    flagged = 0
+    by_expert = {}
+    for job, gp in zip(jobs, gap_list):
+        if gp.any():
+            flagged += int(np.count_nonzero(gp))
+            by_expert.setdefault((job[0], job[1]), []).append((job[2], job[3], gp))
+    for (which, e), items in by_expert.items():
+        d = L["experts"] if which == "routed" else L["shared"]
+        fmt = c["fmt"] if which == "routed" else "f16"
+        wd = _abs_rows(fmt, d["down"][e], None if d.get("down_s") is None else d["down_s"][e])
+        for q, wt, gp in items:
+            nz = np.nonzero(gp)[0]
+            allow[q] += wt * (wd[:, nz].astype(np.float64) @ gp[nz])
+    return allow, flagged
+
+
 def check_outputs(y_gpu_f64, y32_gpu_f64, y_ref_bits_f64, y32_ref_f64, adt, max_abs=2e-2, rel_l2=1e-3,
-                  flip_bound=None):
+                  allow=None):
     """The parity bar: f32 outputs within max-abs and rel-L2; 16-bit outputs within the same
     bars, except that an element may differ by one unit in the last place of the 16-bit type
     (both sides round an f32 sum; sums a hair apart can straddle a rounding boundary).
 
-    flip_bound: both sides also round the intermediate h to 16 bits; where an h element sits
-    next to a rounding boundary the two sides can round it to neighbouring values, which moves
-    the outputs that depend on it by up to ulp16(h) * |W_d| -- one such flip shifts a whole
-    output row of that token.  With flip_bound set, elements beyond max_abs are accepted if they
-    are at most 2 % of the outputs and each stays within flip_bound; rel-L2 is never relaxed."""
+    allow: per-output allowance from flip_allowance (the h elements next to a 16-bit rounding
+    boundary, named by the oracle).  An output beyond max_abs is accepted only if its deviation
+    is covered by its own allowance (plus OUT_SLACK for the f32 arithmetic beside it); rel-L2 is
+    never relaxed."""
     def within(a, b, extra):
         d = np.abs(a - b)
-        allow = np.maximum(max_abs, extra)
-        bad = d > allow
-        if flip_bound is not None and bad.any():
-            ok = bad.sum() <= max(1, int(0.02 * d.size)) and np.all(d[bad] <= flip_bound)
-            return ok, float(d.max()), int(bad.sum())
+        bar = np.maximum(max_abs, extra)
+        if allow is not None:
+            bar = np.maximum(bar, allow + OUT_SLACK + extra)
+        bad = d > bar
         return not bad.any(), float(d.max()), int(bad.sum())
     ok, dmax, nbad = within(y32_gpu_f64, y32_ref_f64, 0.0)
     rel = np.linalg.norm(y32_gpu_f64 - y32_ref_f64) / max(np.linalg.norm(y32_ref_f64), 1e-30)
@@ -146,25 +242,3 @@ def check_outputs(y_gpu_f64, y32_gpu_f64, y_ref_bits_f64, y32_ref_f64, adt, max_
     rel16 = np.linalg.norm(y_gpu_f64 - y_ref_bits_f64) / max(np.linalg.norm(y_ref_bits_f64), 1e-30)
     assert rel16 <= rel_l2, ("16-bit rel-L2", rel16)
     return dmax, rel
-
-
-def h_flip_bound(oex, xin_f64_rows, idx_rows, adt, down_f64_absmax):
-    """2 * ulp16(max |h|) * max |W_d|: the most two neighbouring-value roundings of h can move
-    one output (routing weights are at most 1).  max |h| from the oracle's own h of the routes."""
-    import oracle
-    hmax = 0.0
-    for xrow, sel in zip(xin_f64_rows, idx_rows):
-        for e in sel:
-            h, _ = oracle.expert_ffn(oex, int(e), xrow, adt)
-            hmax = max(hmax, float(np.abs(h).max()))
-    return 2.0 * float(ulp16(hmax, adt)) * down_f64_absmax
-
-
-def weight_absmax(fmt, codes, scales=None):
-    """An upper bound of |W| over a canonical weight tensor, computed without dequantising it."""
-    if fmt in ("f16", "bf16"):
-        return float(codes.abs().max().item())
-    if fmt == "mxfp4":
-        return 6.0 * 2.0 ** (int(scales.max().item()) - 127)
-    sm = scales.float()
-    return float(torch.maximum(sm[..., 1].abs(), (15.0 * sm[..., 0] + sm[..., 1]).abs()).max().item())

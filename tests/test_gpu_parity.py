@@ -13,8 +13,8 @@ import torch
 
 import oracle
 from mixture_experts_routed_logits_gb300 import synth
-from tests._helpers import (bits16, check_outputs, gpu_layer, h_flip_bound, oracle_layer,
-                            oracle_route, parity_metrics, to_device, weight_absmax)
+from tests._helpers import (bits16, check_outputs, flip_allowance, gpu_layer, kappa_for, oracle_layer,
+                            oracle_route, parity_metrics, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -146,15 +146,11 @@ def _forward_parity(case, path):
     rows = slice(None) if toks is None else toks
     g32 = y32.double().cpu().numpy()[rows]
     gy = oracle.adt_bits_to_f64(bits16(y)[rows], c["adt"])
-    fb = None
-    if toks is not None:
-        # large case: bound the effect of h rounding flips from the oracle's own h
-        ex_d = L["experts"]
-        wd_max = weight_absmax(c["fmt"], ex_d["down"], ex_d.get("down_s"))
-        fb = h_flip_bound(oex, oracle.adt_bits_to_f64(xin[toks][:2], c["adt"]), oidx[toks][:2],
-                          c["adt"], wd_max)
+    # h elements next to a 16-bit rounding boundary (named by the oracle) and what they may move
+    allow, _ = flip_allowance(L, oex, osh, oracle.adt_bits_to_f64(xin[rows], c["adt"]), oidx[rows],
+                              ow[rows], c["adt"], kappa=kappa_for(c, T, path), nthreads=NTHREADS)
     check_outputs(gy, g32, oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"],
-                  MAX_ABS, REL_L2, flip_bound=fb)
+                  MAX_ABS, REL_L2, allow=allow)
     assert moe.device_status(ws) == 0
 
 

@@ -9,8 +9,8 @@ import torch
 
 import oracle
 from mixture_experts_routed_logits_gb300 import synth
-from tests._helpers import (bits16, check_outputs, gpu_layer, h_flip_bound, oracle_layer, oracle_route,
-                            to_device, weight_absmax)
+from tests._helpers import (bits16, check_outputs, flip_allowance, gpu_layer, kappa_for, oracle_layer, oracle_route,
+                            to_device)
 
 pytestmark = pytest.mark.gpu
 NTHREADS = max(1, min(16, os.cpu_count() or 1))
@@ -71,16 +71,12 @@ def test_tc_gemm_parity(case):
     toks = None if (T <= 48 and shapes is not None) else np.unique(np.linspace(0, T - 1, 6).astype(np.int32))
     oy, oy32, _ = oracle.moe_forward(xb, c["adt"], oex, oidx, ow, tokens=toks, nthreads=NTHREADS)
     rows = slice(None) if toks is None else toks
-    fb = None
-    if toks is not None:
-        # large case: bound the effect of h rounding flips from the oracle's own h
-        ex_d = L["experts"]
-        wd_max = weight_absmax(c["fmt"], ex_d["down"], ex_d.get("down_s"))
-        xin = oracle.adt_bits_to_f64(xb[toks], c["adt"])
-        fb = h_flip_bound(oex, xin[:2], oidx[toks][:2], c["adt"], wd_max)
+    # h elements next to a 16-bit rounding boundary (named by the oracle) and what they may move
+    allow, _ = flip_allowance(L, oex, None, oracle.adt_bits_to_f64(xb[rows], c["adt"]), oidx[rows],
+                              ow[rows], c["adt"], kappa=kappa_for(c, T, "gemm"), nthreads=NTHREADS)
     check_outputs(oracle.adt_bits_to_f64(bits16(y)[rows], c["adt"]), y32.double().cpu().numpy()[rows],
                   oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"],
-                  flip_bound=fb)
+                  allow=allow)
 
 
 @pytest.mark.parametrize("case", [(5, 8, dict(H=512, I=1024, E=8, k=2)), (5, 64, dict(H=256, I=512, E=8, k=2)),
