@@ -224,17 +224,28 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
  * they run.  It calls no allocator (no cudaMalloc, no cudaFree).
  *   - Calls that need more scratch than 16 MiB (ts_moe_workspace_size) return
  *     TS_ERR_WORKSPACE and launch nothing.
- *   - The first call on each device looks up the scratch's device address
- *     (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *   - The first call on each device (and the first after a device reset) looks up the
+ *     scratch's device address (cudaGetSymbolAddress) and caches it for the current CUDA
+ *     context; make that first call before any stream capture.
  *   - Every call on a device shares the one scratch array and it keeps the last call's
  *     contents; the call clears what must start at zero (the device status word) itself.
  *     Calls that overlap on the GPU (different streams, no ordering between them) race on the
  *     scratch and produce wrong results: order them on one stream or use ts_moe_forward.
+ *   - Device-side failures of the call (a bounded wait that expired, an expert id outside
+ *     0..E-1, an MXFP4 scale outside the tensor-core path's range) are reported through the
+ *     scratch's status word: read them with ts_moe_noalloc_device_status.
  * Other arguments as ts_moe_forward.                                                        */
 ts_status ts_moe_forward_noalloc(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
                                  const int32_t* idx, const float* w, int32_t k,
                                  const ts_moe_experts* shared, void* y, float* y_f32,
                                  void* stream);
+
+/* Reads (synchronously, on `stream`) and clears the device status word of the scratch that
+ * ts_moe_forward_noalloc uses on the current device: *code = 0 when the last such call (every
+ * call clears the word when it starts) reported nothing, else a TS_ERR_* value.  The source
+ * pages have no counterpart; it is the status read of ts_moe_device_status for callers that
+ * hold no workspace.                                                                        */
+ts_status ts_moe_noalloc_device_status(int32_t* code, void* stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* After step 5 (Gemma layers): the sandwich tail.                                             */
@@ -268,6 +279,16 @@ const char* ts_last_error(void);
  * ts_moe_forward set when a bounded wait expires or a device-side check fails.
  * *code = 0 when nothing was reported; otherwise a TS_ERR_* value.                          */
 ts_status ts_moe_device_status(void* ws, int32_t* code, void* stream);
+
+/* Exercises the bounded waits (test use; the pages' counterpart is the refusal convention:
+ * fail with a status, never hang or degrade).  mode 1: the next ts_moe_forward* call on this
+ * thread that runs the streaming GEMV expert path withholds the first weight copy of its
+ * phase-1 launch, so that launch's consumer warps wait on a copy that never arrives; their
+ * bounded wait (about 2^31 SM clocks, a second) runs out, they report TS_ERR_TIMEOUT through
+ * the device status word (ts_moe_device_status), the launch drains the copies it did issue and
+ * returns, and the call's outputs are meaningless.  The setting is consumed by the next
+ * forward call whichever path it takes.  mode 0 clears it.                                  */
+ts_status ts_moe_set_wait_test(int32_t mode);
 
 /* Per-phase timing (the counterpart of the pages' PhaseCounters / per-command-buffer GPU
  * time).  Registers, for the calling thread, up to 8 cudaEvent_t handles (host array, copied;

@@ -74,6 +74,8 @@ def lib():
             "ts_moe_device_status": ([vp, ctypes.POINTER(i32), vp], ctypes.c_int),
             "ts_moe_forward_noalloc": ([vp, i32, i32, pe, vp, vp, i32, pe, vp, vp, vp],
                                        ctypes.c_int),
+            "ts_moe_noalloc_device_status": ([ctypes.POINTER(i32), vp], ctypes.c_int),
+            "ts_moe_set_wait_test": ([i32], ctypes.c_int),
             "ts_moe_set_phase_events": ([ctypes.POINTER(vp), i32], ctypes.c_int),
             "ts_moe_gemma_tail": ([vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, vp], ctypes.c_int),
         }
@@ -281,7 +283,20 @@ def set_phase_events(events):
     check(lib().ts_moe_set_phase_events(arr, len(events)))
 
 
+def set_wait_test(mode):
+    """1: the next forward() on this thread withholds its GEMV phase-1 launch's first weight
+    copy, so a bounded wait runs out and the device status reports TS_ERR_TIMEOUT (test use)."""
+    check(lib().ts_moe_set_wait_test(int(mode)))
+
+
 def device_status(ws, stream=None):
     code = ctypes.c_int32(0)
     check(lib().ts_moe_device_status(_ptr(ws), ctypes.byref(code), _stream(stream)))
+    return code.value
+
+
+def noalloc_device_status(stream=None):
+    """Reads and clears the status word of the scratch forward_noalloc uses on this device."""
+    code = ctypes.c_int32(0)
+    check(lib().ts_moe_noalloc_device_status(ctypes.byref(code), _stream(stream)))
     return code.value

@@ -11,9 +11,15 @@
 // The scratch is a file-scope __device__ array of kScratchBytes (16 MiB).  Every GPU on which
 // this code is loaded keeps that array until the process exits.  Host code cannot use the
 // array's name as a device address (on the host it is only a stand-in symbol), so its device
-// address is looked up once per device with cudaGetSymbolAddress and cached.  That lookup
-// happens inside the first call on each device.
+// address is looked up with cudaGetSymbolAddress, with the device current, and cached per
+// device.  The cache entry remembers the id of the CUDA context it was looked up in: a device
+// reset destroys that context (and the module's copy of the array with it), and the next call
+// finds a new context id and looks the address up again.  The cache is filled under a mutex,
+// so host threads may call concurrently (their GPU work still races, see ts_moe.h).
+#include <cuda.h>
+
 #include <cstdio>
+#include <mutex>
 
 #include "../../include/ts_moe.h"
 #include "internal.h"
@@ -28,21 +34,61 @@ constexpr size_t kScratchBytes = static_cast<size_t>(16) << 20;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-// Device address of g_scratch on the current device (looked up once per device).
+// Id of the calling thread's current CUDA context (0 if none is current or the driver cannot
+// say), through the driver entry points the runtime hands out.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_scratch on the current device, in the current context.
 cudaError_t scratch_address(void** out) {
-    static void* addr[64] = {nullptr};
+    struct Slot { unsigned long long ctx; void* addr; };
+    static Slot slots[64];
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess) return e;
-        addr[dev] = p;
+    std::lock_guard<std::mutex> lock(mu);
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && slots[dev].ctx == ctx && slots[dev].addr) {
+        *out = slots[dev].addr;
+        return cudaSuccess;
     }
-    *out = addr[dev];
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);      // makes the device's context current if needed
+    if (e != cudaSuccess) return e;
+    slots[dev].ctx = current_context_id();
+    slots[dev].addr = p;
+    *out = p;
     return cudaSuccess;
+}
+
+ts_status cuda_error(const char* what, cudaError_t e) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    (void)cudaGetLastError();
+    return record_error(TS_ERR_CUDA, msg);
 }
 
 }  // namespace
@@ -71,12 +117,17 @@ extern "C" ts_status ts_moe_forward_noalloc(const void* x, int32_t adt, int32_t 
     cudaError_t e = scratch_address(&scratch);
     // the first word of the scratch is the device status word: start every call from zero
     if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        snprintf(msg, sizeof(msg), "ts_moe_forward_noalloc: %s (%s)", cudaGetErrorName(e),
-                 cudaGetErrorString(e));
-        (void)cudaGetLastError();
-        return record_error(TS_ERR_CUDA, msg);
-    }
+    if (e != cudaSuccess) return cuda_error("ts_moe_forward_noalloc", e);
     return ts_moe_forward(x, adt, T, ex, idx, w, k, shared, y, y_f32, scratch, kScratchBytes,
                           stream);
+}
+
+// The status word of the scratch (its first int) is where the kernels of the last
+// ts_moe_forward_noalloc call on this device reported a device-side failure.
+extern "C" ts_status ts_moe_noalloc_device_status(int32_t* code, void* stream) {
+    if (!code) return record_error(TS_ERR_INVALID_ARG, "ts_moe_noalloc_device_status: code is NULL");
+    void* scratch = nullptr;
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) return cuda_error("ts_moe_noalloc_device_status", e);
+    return ts_moe_device_status(scratch, code, stream);
 }

@@ -58,6 +58,47 @@ def test_noalloc_matches_forward_two_calls_in_a_row():
     for (c, *_), (ry, ry32), (ny, ny32) in zip(layers, refs, outs):
         check_outputs(_as_f64(ny, c["adt"]), ny32.double().cpu().numpy(), _as_f64(ry, c["adt"]),
                       ry32.double().cpu().numpy(), c["adt"])
+    assert moe.noalloc_device_status() == 0
+
+
+def test_noalloc_scratch_reuse_across_every_expert_path():
+    """Calls of different shapes and paths back to back on the one scratch: the tensor-core
+    grouped GEMM (T > 8; T*k <= 64 keeps split-K partials and counters in the scratch), the
+    decode GEMV with the route list and combine fused in, and the GEMV with the route-list
+    kernel and a separate combine (T*k > 512).  Each result equals ts_moe_forward's bit for bit
+    (same kernels, deterministic), including a repeat of the first call after the others."""
+    import mixture_experts_routed_logits_gb300 as moe
+    layers = [_layer(2, 16, dict(H=256, I=256, E=8, k=4)),                      # MXFP4, GEMM, split K
+              _layer(2, 5, dict(H=512, I=384, E=8, k=4)),                       # MXFP4, fused GEMV
+              _layer(2, 40, dict(H=256, I=256, E=8, k=4)),                      # MXFP4, GEMM
+              _layer(4, 80, dict(H=256, I=96, E=16, k=8, shared_I=128)),        # INT4 GEMV, T*k > 512
+              _layer(2, 16, dict(H=256, I=256, E=8, k=4))]                      # the first again
+    layers[4] = layers[0]
+    refs = [moe.forward(x, ex, idx, w, shared=sh, want_f32=True) for c, x, ex, sh, idx, w in layers]
+    outs = []
+    for c, x, ex, sh, idx, w in layers:
+        outs.append(moe.forward_noalloc(x, ex, idx, w, shared=sh, want_f32=True))
+    torch.cuda.synchronize()
+    for (ry, ry32), (ny, ny32) in zip(refs, outs):
+        assert torch.equal(ny.view(torch.int16), ry.view(torch.int16))
+        assert torch.equal(ny32.view(torch.int32), ry32.view(torch.int32))
+    assert moe.noalloc_device_status() == 0
+
+
+def test_noalloc_reports_device_errors():
+    """An expert id outside 0..E-1 is left out of the route list and reported through the
+    scratch's status word, which ts_moe_noalloc_device_status reads and clears."""
+    import mixture_experts_routed_logits_gb300 as moe
+    c, x, ex, sh, idx, w = _layer(2, 5, dict(H=512, I=384, E=8, k=4))
+    bad = idx.clone()
+    bad[1, 2] = c["E"] + 3
+    moe.forward_noalloc(x, ex, bad, w, shared=sh)
+    torch.cuda.synchronize()
+    assert moe.noalloc_device_status() == 1
+    assert moe.noalloc_device_status() == 0          # read and cleared
+    moe.forward_noalloc(x, ex, idx, w, shared=sh)
+    torch.cuda.synchronize()
+    assert moe.noalloc_device_status() == 0
 
 
 def test_noalloc_rejects_work_beyond_its_scratch():
