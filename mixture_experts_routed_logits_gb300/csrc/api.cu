@@ -20,6 +20,7 @@ namespace {
 thread_local std::string g_err;
 thread_local cudaEvent_t g_phase_ev[8];
 thread_local int g_phase_n = 0;
+thread_local int g_wait_test = 0;   // ts_moe_set_wait_test: consumed by the next forward call
 
 // records phase event i (if registered) on the stream; capture-safe
 cudaError_t phase_mark(int i, cudaStream_t st) {
@@ -437,6 +438,8 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     g.cmb_mode = fused ? 1 : 0;
     g.cmb_cnt = cmb;
     g.cmb_n = ex->H / kRowTile;
+    g.stall = g_wait_test;
+    g_wait_test = 0;
     if (!use_gemm) {
         if ((s = launch_gemv_checked(g, st, "ts_moe_forward: expert phase 1")) != TS_OK) return s;
         if ((e = phase_mark(1, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
@@ -462,6 +465,7 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         gs.dense = 1;
         gs.k = 1;
         gs.cmb_mode = 0;
+        gs.stall = 0;
         if ((s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 1")) != TS_OK) return s;
         if ((e = phase_mark(2, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
         gs.phase = 1;
@@ -489,6 +493,7 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     g.in = reinterpret_cast<const uint16_t*>(W + L.h);
     g.out = W + L.e;
     g.cmb_mode = fused ? 2 : 0;
+    g.stall = 0;
     g.w = w;
     g.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
     g.y = y;
@@ -521,6 +526,13 @@ ts_status ts_moe_forward(const void* x, int32_t adt, int32_t T, const ts_moe_exp
                          size_t ws_bytes, void* stream) {
     return ts_moe_forward_path(x, adt, T, ex, idx, w, k, shared, y, y_f32, ws, ws_bytes,
                                TS_PATH_AUTO, stream);
+}
+
+ts_status ts_moe_set_wait_test(int32_t mode) {
+    g_err.clear();
+    if (mode != 0 && mode != 1) return fail(TS_ERR_INVALID_ARG, "ts_moe_set_wait_test: mode=%d not 0 or 1", mode);
+    g_wait_test = mode;
+    return TS_OK;
 }
 
 ts_status ts_moe_set_phase_events(void* const* events, int32_t n) {

@@ -405,6 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         // ================================ producer warp =====================================
         int it = 0, slot = 0;
         uint32_t ph = 0;                // phase parity of the ring slot `slot`
+        int issued[kMaxStages];         // lane 0: the last iteration copied into each slot
+#pragma unroll
+        for (int q = 0; q < kMaxStages; ++q) issued[q] = -1;
         UnitCursor cu;
         cu.seek(u0, RTu, c.goff, nt);
         int pj = -1, e = 0;
@@ -435,6 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     }
                     __syncwarp();
                     if (c.misc[1]) continue;
+                    // test setting: the first stage's copy is withheld, so the consumers'
+                    // bounded wait on it runs out (reported as TS_ERR_TIMEOUT)
+                    if (a.stall && it == 0) continue;
+                    if (lane == 0) issued[s] = it;
                     unsigned char* dst = c.ring + static_cast<size_t>(s) * kStageBytes;
                     if (kPacked) {
                         if (lane == 0) {
@@ -458,10 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 }
             }
         }
-        // if the consumers gave up, wait (bounded) for the copies still in flight
+        // if the consumers gave up, wait (bounded) for the copies still in flight: the last
+        // copy issued into each slot (the slot's barrier has started no later phase)
         if (c.misc[1] && lane == 0) {
-            for (int q = (it > p.nstages ? it - p.nstages : 0); q < it; ++q)
-                mbar_wait_bounded(&c.full[q % p.nstages], (q / p.nstages) & 1);
+            for (int q = 0; q < p.nstages; ++q)
+                if (issued[q] >= 0) mbar_wait_bounded(&c.full[q], (issued[q] / p.nstages) & 1);
         }
         return;
     }

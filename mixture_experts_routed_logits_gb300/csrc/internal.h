@@ -76,6 +76,7 @@ struct GemvArgs {
     const float* seed;            // combine: shared-expert output [T][H] or nullptr
     void* y;                      // combine: [T][H] adt
     float* y_f32;                 // combine: [T][H] or nullptr
+    int stall;                    // test setting: withhold the first weight copy (see api.cu)
 };
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s);
 
