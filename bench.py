@@ -40,10 +40,12 @@ def parse():
     p.add_argument("--T", type=int, default=None)
     p.add_argument("--layers", type=int, default=None, help="rotating weight sets")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm"],
+    p.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm", "gemm_dequant"],
                    help="expert path passed to ts_moe_forward_path")
     p.add_argument("--gemma-tail", action="store_true",
                    help="append the Gemma sandwich tail (ts_moe_gemma_tail) to every step")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="measure only the selected configuration (no per_config entries)")
     p.add_argument("--profile", action="store_true",
                    help="short run for profiler captures: one timed repetition, few samples")
     return p.parse_args()
@@ -216,7 +218,7 @@ def run_reference(args, cfg_id, T, rank, ws):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": c["name"], "T": T, "sample_tokens_per_step": ntok},
+            "config": {"workload": workload_name(c, T), "T": T, "sample_tokens_per_step": ntok},
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": min(cores, ntok),
                              "kind": "oracle",
                              "sample": f"first {ntok} of the {T} tokens of the batch per step, "
@@ -253,30 +255,40 @@ def cpu_baseline(cfg_id, T):
                       f"{dt:.1f} s"}
 
 
-def main():
-    args = parse()
-    ws, rank, local = dist_setup(args)
-    cfg_id = args.config
-    T = args.T or DEFAULT_T[cfg_id]
-    if args.impl == "reference":
-        run_reference(args, cfg_id, T, rank, ws)
-        return
+def workload_name(cfg, T):
+    """Workload label of a configuration at T tokens (the same string on both bench arms)."""
+    import re
+    base = re.sub(r"_T\d+", "", cfg["name"])
+    prefix, rest = base.split("_H", 1)
+    return f"{prefix}_T{T}_H{rest}"
 
+
+def dtype_label(cfg, gemm_path, mx_path=False):
+    """The arithmetic the path computes in (inputs -> multiply -> accumulate)."""
+    fmt, adt = cfg["fmt"], cfg["adt"]
+    if mx_path:
+        return f"{adt}-in/exact 2-term e4m3 split·e2m1, e8m0 block scales, tcgen05 mma/f32-acc"
+    if gemm_path:
+        if fmt == "mxfp4":
+            return f"{adt}-in/f16(exact prescale)·e2m1→f16 tcgen05 mma/f32-acc"
+        return f"{adt}·{fmt} tcgen05 mma/f32-acc"
+    if fmt in ("mxfp4", "int4"):
+        w = "e2m1" if fmt == "mxfp4" else "int4-affine"
+        return f"{adt}-in/f16(exact prescale)·{w} mma.sync/f32-acc"
+    if fmt == "bf16":
+        return "bf16·bf16 mma.sync/f32-acc"
+    return f"{adt}-in/f16·f16 mma.sync/f32-acc"
+
+
+def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min_wall, want_e2e):
+    """Builds the layers of one configuration, captures a CUDA graph per layer and times K-step
+    loops of graph replays (L2 flushed between steps) under clock sampling; returns the
+    configuration's measurement (rank-local time and the slowest rank's)."""
     import numpy as np
     import torch
-    torch.cuda.set_device(local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    import __graft_entry__
-    if rank == 0:
-        __graft_entry__.build()
-    if ws > 1:
-        torch.distributed.barrier()
     import mixture_experts_routed_logits_gb300 as moe
     from mixture_experts_routed_logits_gb300 import synth
 
-    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
     cfg = dict(synth.CONFIGS[cfg_id])
     cfg["T"] = T
     H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["k"]
@@ -349,12 +361,16 @@ def main():
     # the library's automatic choice: tensor-core grouped GEMM above 8 tokens for MXFP4 and for
     # 16-bit weights of the activation type (H, I multiples of 64), else the streaming GEMV
     gemm_ok = H % 64 == 0 and I % 64 == 0 and (cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"])
-    gemm_path = gemm_ok and (args.path == "gemm" or (args.path == "auto" and T > 8))
+    mx_ok = cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
+    gemm_path = (gemm_ok or mx_ok) and (args.path in ("gemm", "gemm_dequant") or (args.path == "auto" and T > 8))
     # GEMV decode (T*k <= 512): router, phase 1, phase 2 (+ fused route list and combine);
     # otherwise router, route list, [gather], phase 1, phase 2, combine; + 2 shared-expert GEMVs
     fused_decode = (not gemm_path) and T * k <= 512
+    # MXFP4 with bf16 activations takes the block-scaled MMA (activation split + two GEMMs);
+    # "gemm_dequant" the f16 MMA over dequantised weights (gather, h conversion)
+    mx_path = gemm_path and cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16" and args.path != "gemm_dequant"
     n_launch_step = ((3 if fused_decode else 5 + (1 if gemm_path else 0)
-                      + (1 if gemm_path and cfg["fmt"] == "mxfp4" else 0))
+                      + (1 if gemm_path and cfg["fmt"] == "mxfp4" and not mx_path else 0))
                      + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail else 0))
 
     def timed(K):
@@ -368,14 +384,14 @@ def main():
         torch.cuda.synchronize()
         return [b[i].elapsed_time(e[i]) for i in range(K)]
 
-    # ---- warm-up + headline timed region ------------------------------------------------------------
+    # ---- warm-up + timed region ---------------------------------------------------------------------
     timed(max(3, args.warmup))
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     # the K-step timed loop is repeated (each repetition exactly K steps, bracketed by
-    # synchronisation) for >= 1.5 s so that the 200 ms clock sampler sees the work; the median
-    # repetition is reported
+    # synchronisation) for >= min_wall seconds so that the 200 ms clock sampler sees the work;
+    # the median repetition is reported
     reps = []
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
@@ -383,7 +399,7 @@ def main():
             torch.cuda.synchronize()
             times = timed(args.steps)
             reps.append(statistics.mean(times))
-            if args.profile or (time.perf_counter() - t_wall0 > 1.5 and len(reps) >= 3):
+            if args.profile or (time.perf_counter() - t_wall0 > min_wall and len(reps) >= 3):
                 break
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall0
@@ -391,7 +407,6 @@ def main():
         torch.distributed.barrier()
     ms = statistics.median(reps)
     ms_max = slowest_rank_ms(ms, ws, "cuda")
-    value = job_tokens_per_s(ws, T, ms_max)
 
     # ---- per-phase breakdown: graphs carrying event-record nodes after every launch ----------------
     # event order in a step: 6 router, 0 route list, 1 phase 1, [2 shared phase 1], 3 phase 2,
@@ -415,7 +430,7 @@ def main():
             prev = phase_ev[j]
     phases = {n: statistics.mean(v) for n, v in samples.items()}
 
-    # ---- algorithmic bytes of the dominant kernel (expert phase 1) ---------------------------------
+    # ---- algorithmic bytes / FLOPs of the dominant kernel (expert phase 1) ---------------------------
     idx_np = layers[0]["idx"].cpu().numpy()
     n_touched = len(np.unique(idx_np))
     fmt = cfg["fmt"]
@@ -436,6 +451,7 @@ def main():
     routes = T * k
     p1_flop = 2.0 * routes * 2 * I * H
     p2_flop = 2.0 * routes * H * I
+    wl = workload_name(cfg, T)
     if gemm_path and fmt != "mxfp4":
         # tensor-bound: FLOPs of the phase-1 grouped GEMM over its launch time, against the
         # sustained bf16 peak (the kernel runs inside a seconds-long loop)
@@ -447,11 +463,11 @@ def main():
         step_tf = (p1_flop + p2_flop) / (ms_max * 1e-3) / 1e12
     else:
         achieved = p1_bytes / (p1_ms * 1e-3) / 1e9
-        traffic = (None if gemm_path else
-                   captured_traffic(f"gemv_{fmt}_phase1",
-                                    cfg["name"].replace("decode_", f"decode_T{T}_")))
+        traffic = None if gemm_path else captured_traffic(f"gemv_{fmt}_phase1", wl)
         roof = {"bound": "hbm",
-                "kernel": ("experts_phase1 (tcgen05 grouped GEMM over packed MXFP4, gate/up)"
+                "kernel": ("experts_phase1 (tcgen05 block-scaled grouped GEMM, MXFP4 gate/up)"
+                           if mx_path else
+                           "experts_phase1 (tcgen05 grouped GEMM over packed MXFP4, gate/up)"
                            if gemm_path else "experts_phase1 (gate/up GEMV)"),
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_source": peak_src,
@@ -459,25 +475,89 @@ def main():
         step_tf = None
 
     # ---- end to end through the public API with host buffers ---------------------------------------
-    ly = layers[0]
-    x_host = ly["L"]["x"].cpu().pin_memory()
-    y_host = torch.empty_like(x_host).pin_memory()
-    x_dev = ly["L"]["x"]
-    e2e_t = []
-    for i in range(max(3, args.warmup) + (3 if args.profile else args.steps)):
-        lyr = layers[i % n_layers]
-        flush.zero_()
-        b = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        b.record()
-        lyr["L"]["x"].copy_(x_host, non_blocking=True)
-        step(lyr)
-        y_host.copy_(lyr["y"], non_blocking=True)
-        e.record()
-        e.synchronize()
-        if i >= max(3, args.warmup):
-            e2e_t.append(b.elapsed_time(e))
-    e2e_ms = statistics.mean(e2e_t)
+    e2e = None
+    if want_e2e:
+        ly = layers[0]
+        x_host = ly["L"]["x"].cpu().pin_memory()
+        y_host = torch.empty_like(x_host).pin_memory()
+        e2e_t = []
+        for i in range(max(3, args.warmup) + (3 if args.profile else args.steps)):
+            lyr = layers[i % n_layers]
+            flush.zero_()
+            b = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            b.record()
+            lyr["L"]["x"].copy_(x_host, non_blocking=True)
+            step(lyr)
+            y_host.copy_(lyr["y"], non_blocking=True)
+            e.record()
+            e.synchronize()
+            if i >= max(3, args.warmup):
+                e2e_t.append(b.elapsed_time(e))
+        e2e_ms = statistics.mean(e2e_t)
+        e2e = {"value": T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
+               "ms_per_step": e2e_ms}
+
+    out = {
+        "ms": ms, "ms_max": ms_max, "value": job_tokens_per_s(ws, T, ms_max), "wall": wall,
+        "n_layers": n_layers, "reps": len(reps), "gemm_path": gemm_path,
+        "n_launch_step": n_launch_step, "n_touched": int(n_touched), "phases": phases,
+        "roofline": roof, "clocks": clk.summary(), "e2e": e2e,
+        "step_tflops": None if step_tf is None else {"TFLOPs": step_tf, "frac": step_tf / bf16_sust},
+        "step_hbm": {"bytes": step_bytes, "GBps": step_bytes / (ms_max * 1e-3) / 1e9,
+                     "frac": step_bytes / (ms_max * 1e-3) / 1e9 / hbm_peak},
+        "dtype": dtype_label(cfg, gemm_path, mx_path), "workload": wl, "cfg": cfg,
+        "path": ("tcgen05 block-scaled grouped GEMM (kind::mxf8f6f4, TMA + TMEM)" if mx_path
+                 else "tcgen05 grouped GEMM (TMA + TMEM)" if gemm_path
+                 else "gemv (mma.sync m16n8k16 over streamed tiles)"),
+    }
+    del layers, graphs, graphs_ev, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+# the other configurations reported beside the headline one (config id, tokens)
+PER_CONFIG = [(1, 4), (2, 1), (3, 512), (4, 8), (5, 2048)]
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    cfg_id = args.config
+    T = args.T or DEFAULT_T[cfg_id]
+    if args.impl == "reference":
+        run_reference(args, cfg_id, T, rank, ws)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if ws > 1:
+        torch.distributed.barrier()
+
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+    m = measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, 1.5, True)
+    cfg = m["cfg"]
+
+    per_config = None
+    if not args.profile and not args.no_per_config and args.config == 2 and args.T is None:
+        per_config = {}
+        for cid, tt in PER_CONFIG:
+            r = measure(cid, tt, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, 0.4, False)
+            per_config[r["workload"]] = {
+                "config": cid, "T": tt, "tokens_per_s": r["value"], "ms_per_step": r["ms_max"],
+                "dtype": r["dtype"], "path": r["path"], "touched_experts": r["n_touched"],
+                "roofline": r["roofline"], "step_hbm": r["step_hbm"], "step_tflops": r["step_tflops"],
+                "phase_ms": r["phases"], "clocks": r["clocks"], "launches_per_step": r["n_launch_step"],
+                "timing": f"{r['reps']} repetitions of {args.steps} steps, median; L2 flushed "
+                          f"between steps; {r['n_layers']} rotating weight sets"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.profile:
@@ -486,36 +566,32 @@ def main():
         except Exception as ex:     # reported, not fatal
             cpu = {"error": str(ex)}
 
-    clocks = clk.summary()
+    H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["k"]
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": m["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms_max"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16" if (fmt in ("mxfp4", "int4", "f16") and not gemm_path) else cfg["adt"],
+        "dtype": m["dtype"],
         "data": "synthetic",
-        "config": {"workload": cfg["name"].replace("decode_", f"decode_T{T}_"), "T": T, "H": H,
-                   "I": I, "E": E, "k": k, "weights": fmt, "activations": cfg["adt"],
-                   "accumulate": "f32",
-                   "path": ("tcgen05 grouped GEMM (TMA + TMEM)" if gemm_path
-                            else "gemv (mma.sync m16n8k16 over streamed tiles)"),
+        "config": {"workload": m["workload"], "T": T, "H": H,
+                   "I": I, "E": E, "k": k, "weights": cfg["fmt"], "activations": cfg["adt"],
+                   "accumulate": "f32", "path": m["path"],
                    "l2": "flushed between timed steps (512 MB write, outside the step events); "
-                         f"{n_layers} rotating weight sets",
+                         f"{m['n_layers']} rotating weight sets",
                    "timing": "CUDA graph per step, CUDA events per step; the K-step loop repeated "
-                             f"{len(reps)}x under clock sampling, median repetition",
-                   "touched_experts": int(n_touched), "parallelism": f"replicas x{ws}",
+                             f"{m['reps']}x under clock sampling, median repetition",
+                   "touched_experts": m["n_touched"], "parallelism": f"replicas x{ws}",
                    "gemma_tail": bool(args.gemma_tail)},
-        "roofline": roof,
-        "step_tflops": None if step_tf is None else {"TFLOPs": step_tf, "frac": step_tf / bf16_sust},
-        "step_hbm": {"bytes": step_bytes, "GBps": step_bytes / (ms_max * 1e-3) / 1e9,
-                     "frac": step_bytes / (ms_max * 1e-3) / 1e9 / hbm_peak},
-        "phase_ms": phases,
+        "roofline": m["roofline"],
+        "step_tflops": m["step_tflops"],
+        "step_hbm": m["step_hbm"],
+        "phase_ms": m["phases"],
         "cpu_baseline": cpu,
-        "e2e": {"value": T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
-                "ms_per_step": e2e_ms},
-        "gpu_launches": n_launch_step * args.steps,
-        "clocks": clocks,
-        "wall_s_timed": wall,
+        "e2e": m["e2e"],
+        "gpu_launches": m["n_launch_step"] * args.steps,
+        "clocks": m["clocks"],
+        "wall_s_timed": m["wall"],
+        "per_config": per_config,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -81,16 +81,25 @@ typedef enum {
                           format has one (MXFP4, or f16/bf16 weights of the activation type)
                           and H, I are multiples of 64, else the GEMV path                      */
     TS_PATH_GEMV = 1,  /* streaming GEMV kernels (any T)                                        */
-    TS_PATH_GEMM = 2   /* tcgen05 grouped GEMM.  MXFP4 weights are dequantised to f16 in shared
-                          memory, exact for e8m0 scales 2^-23..2^13; a block outside that range
-                          makes ts_moe_device_status report TS_ERR_UNSUPPORTED               */
+    TS_PATH_GEMM = 2,  /* tcgen05 grouped GEMM.  MXFP4 weights with bf16 activations and the
+                          tensor-core blobs present (gateup_mx/down_mx): block-scaled MMA
+                          (kind::mxf8f6f4, e2m1 x e4m3 with e8m0 scales; activations split
+                          exactly into two e4m3 terms).  Otherwise as TS_PATH_GEMM_DEQUANT      */
+    TS_PATH_GEMM_DEQUANT = 3  /* tcgen05 grouped GEMM on 16-bit operands: 16-bit weights of the
+                          activation type as they are; MXFP4 weights dequantised to f16 in
+                          shared memory, exact for e8m0 scales 2^-23..2^13 (a block outside
+                          that range makes ts_moe_device_status report TS_ERR_UNSUPPORTED)    */
 } ts_path;
 
 /* One set of experts (routed experts, or the shared expert with E = 1).
  * Requirements: H, I multiples of 32 (and of 16 rows); 1 <= E <= 256.
  * gate_b/up_b ([E][I]) and down_b ([E][H]) are bfloat16 device arrays or NULL (no bias;
  * the pages derive has_bias from a non-zero bias offset).  swiglu_limit / swiglu_alpha are
- * read only for TS_ACT_GPTOSS_SWIGLU (gpt-oss: 7.0 and 1.702).                               */
+ * read only for TS_ACT_GPTOSS_SWIGLU (gpt-oss: 7.0 and 1.702).
+ * gateup_mx/down_mx: MXFP4 only, optional (NULL = absent): the same matrices in the
+ * tensor-core layout written by ts_moe_pack_mx (256-byte aligned device blobs; gateup_mx holds
+ * gate and up together, pair = 1); with them, bf16 activations take the block-scaled
+ * tensor-core path for more than 8 tokens.                                                   */
 typedef struct ts_moe_experts {
     int32_t fmt;   /* ts_wfmt */
     int32_t act;   /* ts_act  */
@@ -103,6 +112,8 @@ typedef struct ts_moe_experts {
     const void* down_b;
     float swiglu_limit;
     float swiglu_alpha;
+    const void* gateup_mx; /* device, ts_moe_pack_mx layout with pair = 1, or NULL */
+    const void* down_mx;   /* device, ts_moe_pack_mx layout with pair = 0, or NULL */
 } ts_moe_experts;
 
 /* ------------------------------------------------------------------------------------------ */
@@ -126,6 +137,29 @@ size_t ts_moe_packed_bytes(int32_t fmt, int32_t nmat, int32_t R, int32_t K);
  * bytes (INT4); tiles of one matrix are contiguous, matrices follow each other.          */
 ts_status ts_moe_pack(int32_t fmt, int32_t nmat, int32_t R, int32_t K, const void* codes,
                       const void* scales, void* packed, size_t packed_bytes, void* stream);
+
+/* Bytes of the tensor-core layout of `nmat` MXFP4 matrices of R rows x K columns (pair = 0),
+ * or of `nmat` gate/up pairs (pair = 1); R % 32 == 0, K % 32 == 0.  0 for unsupported
+ * arguments.                                                                                  */
+size_t ts_moe_packed_mx_bytes(int32_t pair, int32_t nmat, int32_t R, int32_t K);
+
+/* Writes the tensor-core layout of canonical MXFP4 weights (codes and e8m0 scales exactly as
+ * ts_moe_pack takes them) for the block-scaled MMA path.  pair = 1: codes0/scales0 are the gate
+ * matrices and codes1/scales1 the up matrices, stored together; pair = 0: one matrix set
+ * (codes1/scales1 ignored).  G = 1 + pair matrices per expert.
+ *   - codes [nmat][KG][G][R][64 bytes], KG = ceil(K / 128): for each group of 128 columns the
+ *     128 codes of a row (canonical nibble order), gate and up of a row group side by side, so
+ *     one tensor copy fetches a stage of both; zero codes past K;
+ *   - at the next 256-byte boundary, the scales in 512-byte atoms [nmat][U][KG][2][512],
+ *     U = ceil(R / 128) for pairs (atom pair = gate, up) or ceil(R / 256) otherwise (atom pair =
+ *     the two 128-row halves of a 256-row block); row r and block b of an atom at byte
+ *     16*(r%32) + 4*(r/32) + b (the order in which tcgen05.cp spreads them over TMEM); scales of
+ *     rows or blocks past the matrix are 1.0.
+ *   blob device, 256-byte aligned, blob_bytes >= ts_moe_packed_mx_bytes(...).  Async on
+ * `stream`; one-time work (untimed), like the pages' repack walk.                            */
+ts_status ts_moe_pack_mx(int32_t pair, int32_t nmat, int32_t R, int32_t K, const void* codes0,
+                         const void* scales0, const void* codes1, const void* scales1, void* blob,
+                         size_t blob_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* Steps 1-2: routing.                                                                         */

@@ -25,7 +25,7 @@ FMT = {"f16": 0, "bf16": 1, "mxfp4": 2, "int4": 3}
 ACT = {"silu": 0, "gelu_tanh": 1, "gptoss": 2}
 MODE = {"softmax_k": 0, "sigmoid_biased": 1, "softmax_k_scaled": 2}
 ADT = {"f16": 0, "bf16": 1}
-PATH = {"auto": 0, "gemv": 1, "gemm": 2}
+PATH = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_dequant": 3}
 STATUS = {0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_UNSUPPORTED", 3: "TS_ERR_CUDA",
           4: "TS_ERR_TIMEOUT", 5: "TS_ERR_WORKSPACE"}
 
@@ -41,7 +41,8 @@ class CExperts(ctypes.Structure):
                 ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
                 ("gate_b", ctypes.c_void_p), ("up_b", ctypes.c_void_p), ("down_b", ctypes.c_void_p),
-                ("swiglu_limit", ctypes.c_float), ("swiglu_alpha", ctypes.c_float)]
+                ("swiglu_limit", ctypes.c_float), ("swiglu_alpha", ctypes.c_float),
+                ("gateup_mx", ctypes.c_void_p), ("down_mx", ctypes.c_void_p)]
 
 
 _lib = None
@@ -62,6 +63,8 @@ def lib():
             "ts_moe_version": ([], ctypes.c_char_p),
             "ts_moe_packed_bytes": ([i32, i32, i32, i32], sz),
             "ts_moe_pack": ([i32, i32, i32, i32, vp, vp, vp, sz, vp], ctypes.c_int),
+            "ts_moe_packed_mx_bytes": ([i32, i32, i32, i32], sz),
+            "ts_moe_pack_mx": ([i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "ts_moe_route": ([vp, vp, vp, i32, i32, i32, i32, vp, vp, vp], ctypes.c_int),
             "ts_moe_router_route": ([vp, i32, i32, i32, vp, i32, i32, f32, vp, vp, i32, i32, vp,
                                      vp, vp, vp, vp], ctypes.c_int),
@@ -129,26 +132,55 @@ def pack(fmt, codes, scales, stream=None):
     return out
 
 
+def packed_mx_bytes(nmat, R, K, pair=False):
+    return lib().ts_moe_packed_mx_bytes(int(pair), nmat, R, K)
+
+
+def pack_mx(codes, scales, codes_up=None, scales_up=None, stream=None):
+    """Tensor-core layout of canonical MXFP4 weights ([nmat][R][K/2] codes + e8m0 scales) for
+    the block-scaled MMA path (ts_moe_pack_mx); with codes_up/scales_up, gate and up together."""
+    import torch
+    nmat, R, half_k = codes.shape
+    K = half_k * 2
+    pair = codes_up is not None
+    nb = packed_mx_bytes(nmat, R, K, pair)
+    if nb == 0:
+        raise TsMoeError(1, f"cannot pack for the tensor cores: R={R} K={K}")
+    out = torch.empty(nb + 256, dtype=torch.uint8, device=codes.device)
+    off = (-out.data_ptr()) % 256
+    out = out[off:off + nb]
+    check(lib().ts_moe_pack_mx(int(pair), nmat, R, K, _ptr(codes.contiguous()), _ptr(scales.contiguous()),
+                               _ptr(None if codes_up is None else codes_up.contiguous()),
+                               _ptr(None if scales_up is None else scales_up.contiguous()),
+                               _ptr(out), nb, _stream(stream)))
+    return out
+
+
 class Experts:
     """Device weights of one expert set plus its C descriptor (tensors are kept alive)."""
 
     def __init__(self, fmt, act, E, H, I, gate, up, down, gate_b=None, up_b=None, down_b=None,
-                 swiglu_limit=7.0, swiglu_alpha=1.702):
+                 swiglu_limit=7.0, swiglu_alpha=1.702, gateup_mx=None, down_mx=None):
         self.fmt, self.act, self.E, self.H, self.I = fmt, act, E, H, I
-        self._keep = [gate, up, down, gate_b, up_b, down_b]
+        self._keep = [gate, up, down, gate_b, up_b, down_b, gateup_mx, down_mx]
+        ptr = lambda t: None if t is None else t.data_ptr()
         self.c = CExperts(FMT[fmt], ACT[act], E, H, I, gate.data_ptr(), up.data_ptr(),
-                          down.data_ptr(), None if gate_b is None else gate_b.data_ptr(),
-                          None if up_b is None else up_b.data_ptr(),
-                          None if down_b is None else down_b.data_ptr(), swiglu_limit,
-                          swiglu_alpha)
+                          down.data_ptr(), ptr(gate_b), ptr(up_b), ptr(down_b), swiglu_limit,
+                          swiglu_alpha, ptr(gateup_mx), ptr(down_mx))
 
     @classmethod
-    def from_canonical(cls, fmt, act, w: dict, stream=None, **kw):
-        """w: gate/up/down (+ _s scales, + _b biases) in the canonical layout, on the GPU."""
+    def from_canonical(cls, fmt, act, w: dict, stream=None, with_mx=True, **kw):
+        """w: gate/up/down (+ _s scales, + _b biases) in the canonical layout, on the GPU.
+        MXFP4 weights also get their tensor-core layout (block-scaled MMA path) unless
+        with_mx is False."""
         gate, up, down = w["gate"], w["up"], w["down"]
+        mx = {}
         if fmt in ("mxfp4", "int4"):
             E, I, half_h = gate.shape
             H = half_h * 2
+            if fmt == "mxfp4" and with_mx:
+                mx = dict(gateup_mx=pack_mx(gate, w["gate_s"], up, w["up_s"], stream=stream),
+                          down_mx=pack_mx(down, w["down_s"], stream=stream))
             gate = pack(fmt, gate, w["gate_s"], stream)
             up = pack(fmt, up, w["up_s"], stream)
             down = pack(fmt, down, w["down_s"], stream)
@@ -156,7 +188,7 @@ class Experts:
             E, I, H = gate.shape
             gate, up, down = gate.contiguous(), up.contiguous(), down.contiguous()
         return cls(fmt, act, E, H, I, gate, up, down, w.get("gate_b"), w.get("up_b"),
-                   w.get("down_b"), **kw)
+                   w.get("down_b"), **mx, **kw)
 
 
 # --------------------------------------------------------------------------------- routing

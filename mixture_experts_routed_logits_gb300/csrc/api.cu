@@ -85,6 +85,10 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
         return fail(TS_ERR_INVALID_ARG, "%s: weight pointers must be 16-byte aligned", what);
     if (!aligned(ex->gate_b, 2) || !aligned(ex->up_b, 2) || !aligned(ex->down_b, 2))
         return fail(TS_ERR_INVALID_ARG, "%s: bias pointers must be 2-byte aligned", what);
+    if (!aligned(ex->gateup_mx, 256) || !aligned(ex->down_mx, 256))
+        return fail(TS_ERR_INVALID_ARG, "%s: tensor-core MXFP4 blobs must be 256-byte aligned", what);
+    if ((ex->gateup_mx || ex->down_mx) && (ex->fmt != FMT_MXFP4 || !ex->gateup_mx || !ex->down_mx))
+        return fail(TS_ERR_INVALID_ARG, "%s: gateup_mx/down_mx are MXFP4 blobs, both or none", what);
     if (ex->fmt == FMT_BF16 && adt != TS_DT_BF16)
         return fail(TS_ERR_UNSUPPORTED,
                     "%s: bf16 weights need bf16 activations (f16 activations would be rounded)", what);
@@ -93,6 +97,7 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
 
 struct WsLayout {
     size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hinv, h16, cmb, part, tcnt, total;
+    size_t xq, xsf, hq, hsf;   // block-scaled path: split activations and their scales
     size_t tcnt_n;        // split-K group counters per phase
     int max_split;        // > 1 when the partials fit (decode sizes)
 };
@@ -124,6 +129,11 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
         L.xinv = take(Tk * 4);
         L.hinv = take(Tk * 4);
         L.h16 = take(Tk * ex->I * 2);
+        // two e4m3 planes and the e8m0 scales of x and of h for the block-scaled path
+        L.xq = take(2 * Tk * ex->H);
+        L.xsf = take(Tk * mx_sf_row(ex->H));
+        L.hq = take(2 * Tk * ex->I);
+        L.hsf = take(Tk * mx_sf_row(ex->I));
     }
     // split-K partials of the tensor-core path for decode-sized calls (few routes, so the few
     // (expert, row block) tiles are cut along K to reach every SM): [part][route][2][rows] f32
@@ -187,6 +197,32 @@ ts_status ts_moe_pack(int32_t fmt, int32_t nmat, int32_t R, int32_t K, const voi
                                 static_cast<const uint8_t*>(scales), static_cast<uint8_t*>(packed),
                                 static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ts_moe_pack");
+    return TS_OK;
+}
+
+size_t ts_moe_packed_mx_bytes(int32_t pair, int32_t nmat, int32_t R, int32_t K) {
+    if ((pair != 0 && pair != 1) || nmat < 1 || R <= 0 || K <= 0 || R % 32 || K % kBlockK) return 0;
+    return mx_blob_bytes(1 + pair, nmat, R, K);
+}
+
+ts_status ts_moe_pack_mx(int32_t pair, int32_t nmat, int32_t R, int32_t K, const void* codes0,
+                         const void* scales0, const void* codes1, const void* scales1, void* blob,
+                         size_t blob_bytes, void* stream) {
+    g_err.clear();
+    const size_t need = ts_moe_packed_mx_bytes(pair, nmat, R, K);
+    if (need == 0)
+        return fail(TS_ERR_INVALID_ARG, "ts_moe_pack_mx: needs pair 0 or 1, nmat >= 1, R %% 32 == 0, "
+                    "K %% 32 == 0 (pair=%d nmat=%d R=%d K=%d)", pair, nmat, R, K);
+    if (!codes0 || !scales0 || !blob || (pair && (!codes1 || !scales1)))
+        return fail(TS_ERR_INVALID_ARG, "ts_moe_pack_mx: NULL pointer");
+    if (!aligned(blob, 256)) return fail(TS_ERR_INVALID_ARG, "ts_moe_pack_mx: blob must be 256-byte aligned");
+    if (blob_bytes < need)
+        return fail(TS_ERR_INVALID_ARG, "ts_moe_pack_mx: blob_bytes %zu < %zu", blob_bytes, need);
+    cudaError_t e = launch_mx_pack(1 + pair, nmat, R, K, static_cast<const uint8_t*>(codes0),
+                                   static_cast<const uint8_t*>(scales0), static_cast<const uint8_t*>(codes1),
+                                   static_cast<const uint8_t*>(scales1), static_cast<uint8_t*>(blob),
+                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_pack_mx");
     return TS_OK;
 }
 
@@ -304,7 +340,7 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
         if (shared->E != 1 || shared->H != ex->H)
             return fail(TS_ERR_INVALID_ARG, "%s: shared expert needs E=1 and H=%d", what, ex->H);
     }
-    if (path < TS_PATH_AUTO || path > TS_PATH_GEMM) return fail(TS_ERR_INVALID_ARG, "%s: bad path %d", what, path);
+    if (path < TS_PATH_AUTO || path > TS_PATH_GEMM_DEQUANT) return fail(TS_ERR_INVALID_ARG, "%s: bad path %d", what, path);
     if (static_cast<long long>(T) * k > (1ll << 24)) return fail(TS_ERR_UNSUPPORTED, "%s: T*k above 2^24", what);
     if (T == 0) return TS_OK;
     if (!x || !idx || !w || !y) return fail(TS_ERR_INVALID_ARG, "%s: x/idx/w/y is NULL", what);
@@ -318,12 +354,18 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
                           (ex->fmt == FMT_F16 && adt == TS_DT_F16);
     const bool gemm_shape = ex->H % 64 == 0 && ex->I % 64 == 0;
     const bool quant_gemm = ex->fmt == FMT_MXFP4;
-    if (path == TS_PATH_GEMM && !((gemm_fmt || quant_gemm) && gemm_shape))
+    // block-scaled MMA: MXFP4 weights with their tensor-core blobs, bf16 activations (two e4m3
+    // terms hold a bf16 value exactly; an f16 value needs more)
+    const bool mx_ok = quant_gemm && adt == TS_DT_BF16 && ex->gateup_mx && ex->down_mx;
+    if ((path == TS_PATH_GEMM && !mx_ok && !((gemm_fmt || quant_gemm) && gemm_shape)) ||
+        (path == TS_PATH_GEMM_DEQUANT && !((gemm_fmt || quant_gemm) && gemm_shape)))
         return fail(TS_ERR_UNSUPPORTED,
                     "%s: the tensor-core path serves MXFP4 weights or 16-bit weights of the "
-                    "activation type, with H %% 64 == 0 and I %% 64 == 0 (fmt=%d adt=%d H=%d I=%d)",
+                    "activation type, with H %% 64 == 0 and I %% 64 == 0 (or MXFP4 with its "
+                    "tensor-core blobs and bf16 activations) (fmt=%d adt=%d H=%d I=%d)",
                     what, ex->fmt, adt, ex->H, ex->I);
-    const bool use_gemm = path == TS_PATH_GEMM ||
+    const bool use_mx = mx_ok && (path == TS_PATH_GEMM || (path == TS_PATH_AUTO && T > 8));
+    const bool use_gemm = use_mx || path == TS_PATH_GEMM || path == TS_PATH_GEMM_DEQUANT ||
                           (path == TS_PATH_AUTO && T > 8 && (gemm_fmt || quant_gemm) && gemm_shape);
 
     unsigned char* W = static_cast<unsigned char*>(ws);
@@ -338,7 +380,57 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     if (e == cudaSuccess) e = phase_mark(0, st);
     if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: route list");
 
-    if (use_gemm) {
+    if (use_mx) {
+        const int sms = num_sms_current();
+        if (sms <= 0) return fail(TS_ERR_CUDA, "%s: no CUDA device", what);
+        const int Tk = T * k;
+        uint8_t* xq = W + L.xq;
+        uint8_t* xsf = W + L.xsf;
+        e = launch_mx_split_rows(static_cast<const uint16_t*>(x), perm, k, ex->H, Tk, xq, xsf, st);
+        if (e == cudaSuccess) e = phase_mark(0, st);
+        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: activation split");
+        MxArgs M{};
+        M.phase = 0;
+        M.act = ex->act;
+        M.limit = ex->swiglu_limit;
+        M.alpha = ex->swiglu_alpha;
+        M.w = static_cast<const uint8_t*>(ex->gateup_mx);
+        M.b0 = static_cast<const uint16_t*>(ex->gate_b);
+        M.b1 = static_cast<const uint16_t*>(ex->up_b);
+        M.R = ex->I;
+        M.K = ex->H;
+        M.E = ex->E;
+        M.bq = xq;
+        M.bsf = xsf;
+        M.rows_in = Tk;
+        M.hq = W + L.hq;
+        M.hsf = W + L.hsf;
+        M.off = off;
+        M.perm = perm;
+        M.status = status;
+        M.max_split = L.max_split;
+        M.part = L.max_split > 1 ? reinterpret_cast<float*>(W + L.part) : nullptr;
+        M.cnt = L.max_split > 1 ? reinterpret_cast<int*>(W + L.tcnt) : nullptr;
+        if (L.max_split > 1) e = cudaMemsetAsync(W + L.tcnt, 0, 2 * L.tcnt_n * 4, st);
+        if (e == cudaSuccess) e = launch_mx_gemm(M, sms, st);
+        if (e == cudaSuccess) e = phase_mark(1, st);
+        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled phase 1");
+        M.phase = 1;
+        M.w = static_cast<const uint8_t*>(ex->down_mx);
+        M.b0 = static_cast<const uint16_t*>(ex->down_b);
+        M.b1 = nullptr;
+        M.R = ex->H;
+        M.K = ex->I;
+        M.bq = W + L.hq;
+        M.bsf = W + L.hsf;
+        M.hq = nullptr;
+        M.hsf = nullptr;
+        M.e_out = reinterpret_cast<float*>(W + L.e);
+        if (L.max_split > 1) M.cnt = reinterpret_cast<int*>(W + L.tcnt) + L.tcnt_n;
+        e = launch_mx_gemm(M, sms, st);
+        if (e == cudaSuccess) e = phase_mark(3, st);
+        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled phase 2");
+    } else if (use_gemm) {
         const int sms = num_sms_current();
         if (sms <= 0) return fail(TS_ERR_CUDA, "%s: no CUDA device", what);
         const int Tk = T * k;

@@ -216,6 +216,19 @@ __device__ __forceinline__ uint32_t u4pair_to_f16x2(uint32_t w, int s) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Gated-FFN activations in f32: SiLU-GLU, gelu-tanh-GLU, and the clamped SwiGLU of gpt-oss
+// (biases already added to g and u; the clamp comes before the gate).
+__device__ __forceinline__ float act_fn(int act, float g, float u, float limit, float alpha) {
+    if (act == ACT_SILU) return g / (1.0f + expf(-g)) * u;
+    if (act == ACT_GELU) {
+        const float c = 0.7978845608028654f;   // sqrt(2/pi)
+        return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g))) * u;
+    }
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
+    return g / (1.0f + expf(-alpha * g)) * (u + 1.0f);
+}
+
 __device__ __forceinline__ float warp_sum_xor(float v) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));

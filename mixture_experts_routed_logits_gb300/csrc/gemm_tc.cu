@@ -35,7 +35,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include "common.cuh"
+#include "tc_common.cuh"
 
 namespace tsmoe {
 
@@ -69,99 +69,6 @@ struct TcParams {
     GemmArgs a;
     TcLayout ly;
 };
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
-// apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1) << 16;             // leading byte offset (unused here)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;     // stride byte offset
-    d |= static_cast<uint64_t>(1) << 46;             // version
-    d |= static_cast<uint64_t>(2) << 61;             // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: D f32, A/B f16 (0) or bf16 (1), both K-major.
-__device__ __forceinline__ uint32_t idesc_f16kind(int ab_bf16, int M, int N) {
-    return (1u << 4) | (static_cast<uint32_t>(ab_bf16) << 7) |
-           (static_cast<uint32_t>(ab_bf16) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                     uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Two 16-column loads (rows of this warp's lane quarter), one wait for both.
-__device__ __forceinline__ void tmem_ld16_pair(uint32_t ta, uint32_t tb, float va[16], float vb[16]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15}, [%32];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
-        "%28,%29,%30,%31}, [%33];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(ta), "r"(tb)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        va[i] = __uint_as_float(r[i]);
-        vb[i] = __uint_as_float(r[16 + i]);
-    }
-}
-
-__device__ __forceinline__ float act_fn(int act, float g, float u, float limit, float alpha) {
-    if (act == ACT_SILU) return g / (1.0f + expf(-g)) * u;
-    if (act == ACT_GELU) {
-        const float c = 0.7978845608028654f;   // sqrt(2/pi)
-        return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g))) * u;
-    }
-    g = fminf(g, limit);
-    u = fminf(fmaxf(u, -limit), limit);
-    return g / (1.0f + expf(-alpha * g)) * (u + 1.0f);
-}
 
 constexpr int kMaxSlots = 8;
 
@@ -701,62 +608,6 @@ __global__ void __launch_bounds__(128) h_to_f16_kernel(const uint16_t* __restric
     if (threadIdx.x == 0) inv_out[p] = inv;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-bool make_map_3d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint64_t R,
-                 uint64_t E, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {K, R, E};
-    const cuuint64_t strides[2] = {K * 2, R * K * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), box_rows, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, dt_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Packed MXFP4 matrices [E][R/16 tiles][K/32 blocks x 272 B] as a 3-D uint32 tensor
-// {68 * nblk, R/16, E}; a {136, 8, 1} box is 8 row tiles x 2 blocks (one 64-column stage).
-bool make_map_packed(CUtensorMap* m, const void* base, uint64_t K, uint64_t R, uint64_t E) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const uint64_t nblk = K / kBlockK;
-    const cuuint64_t dims[3] = {nblk * (kPackBlk / 4), R / kRowTile, E};
-    const cuuint64_t strides[2] = {nblk * kPackBlk, (R / kRowTile) * nblk * kPackBlk};
-    const cuuint32_t box[3] = {2 * (kPackBlk / 4), 8, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool make_map_2d(CUtensorMap* m, const void* base, int dt_bf16, uint64_t K, uint64_t rows,
-                 uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {K, rows};
-    const cuuint64_t strides[1] = {K * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(m, dt_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int k, int H, int n,
@@ -811,7 +662,10 @@ static TcLayout tc_layout(const GemmArgs& a, int num_sms, size_t* smem) {
         int S = static_cast<int>((4LL * num_sms + tiles - 1) / tiles);
         if (S > a.max_split) S = a.max_split;
         if (S > nkb / 4) S = nkb / 4;
-        L.S = S < 1 ? 1 : S;
+        if (S < 1) S = 1;
+        // parts of ceil(nkb / S) stages; no part may be left without a stage
+        const int kbp = (nkb + S - 1) / S;
+        L.S = (nkb + kbp - 1) / kbp;
     }
     *smem = 1024 + L.a_ring_bytes + static_cast<size_t>(L.nslot) * L.slot_bytes + kTailBytes;
     return L;
@@ -827,15 +681,15 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     P.ly = tc_layout(a, num_sms, &smem);
     if (P.ly.nslot < 2) return cudaErrorInvalidValue;
     if (!a.quant) {
-        if (!make_map_3d(&P.tmA0, a.w0, a.ab_bf16, KA, Rm, a.E, kBM)) return cudaErrorInvalidValue;
-        if (!make_map_3d(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, a.ab_bf16, KA, Rm, a.E, kBM))
+        if (!make_map_3d(&P.tmA0, a.w0, a.ab_bf16, KA, Rm, a.E, kBK, kBM)) return cudaErrorInvalidValue;
+        if (!make_map_3d(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, a.ab_bf16, KA, Rm, a.E, kBK, kBM))
             return cudaErrorInvalidValue;
     } else {
-        if (!make_map_packed(&P.tmA0, a.w0, KA, Rm, a.E)) return cudaErrorInvalidValue;
-        if (!make_map_packed(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, KA, Rm, a.E))
+        if (!make_map_packed(&P.tmA0, a.w0, KA, Rm, a.E, kPackBlk)) return cudaErrorInvalidValue;
+        if (!make_map_packed(&P.tmA1, a.phase == 0 ? a.w1 : a.w0, KA, Rm, a.E, kPackBlk))
             return cudaErrorInvalidValue;
     }
-    if (!make_map_2d(&P.tmB, a.act_in, a.ab_bf16, KA, a.rows_in, 64)) return cudaErrorInvalidValue;
+    if (!make_map_2d(&P.tmB, a.act_in, a.ab_bf16, KA, a.rows_in, kBK, 64)) return cudaErrorInvalidValue;
     cudaError_t e;
     if (a.quant) {
         e = ensure_smem(tc_gemm_kernel<true>, smem);

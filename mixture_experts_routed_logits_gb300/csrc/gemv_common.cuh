@@ -7,17 +7,6 @@
 namespace tsmoe {
 namespace {
 
-__device__ __forceinline__ float act_fn(int act, float g, float u, float limit, float alpha) {
-    if (act == ACT_SILU) return g / (1.0f + expf(-g)) * u;
-    if (act == ACT_GELU) {
-        const float c = 0.7978845608028654f;   // sqrt(2/pi)
-        return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g))) * u;
-    }
-    g = fminf(g, limit);
-    u = fminf(fmaxf(u, -limit), limit);
-    return g / (1.0f + expf(-alpha * g)) * (u + 1.0f);
-}
-
 // Stages one activation row into shared memory in the mma operand type: f16 with a
 // power-of-two prescale (max |x| * 2^ks in [2^14, 2^15)) when bf16 activations feed the f16
 // mma, else the bits as they are; element order inside each 8-group is natural, or

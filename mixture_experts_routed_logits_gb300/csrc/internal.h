@@ -138,6 +138,63 @@ cudaError_t launch_gather_rows_f16(const uint16_t* x, int adt, const int32_t* pe
 cudaError_t launch_h_to_f16(const uint16_t* h, int adt, int I, int n,
                             uint16_t* h16, float* inv, cudaStream_t s);
 
+// ------------------------------------------------------------------------------------------
+// block-scaled tensor-core path for MXFP4 weights and bf16 activations (gemm_mx.cu)
+// ------------------------------------------------------------------------------------------
+// Tensor-core MXFP4 blob of one group of expert matrices [E][R][K]: G = 2 for gate and up of
+// the same rows (phase 1 uses them together), G = 1 for down.
+//   codes  [E][KG][G][R][64 B], KG = ceil(K / 128): the 128 codes of one row and one group of
+//          128 columns (64 bytes), zero codes past K;
+//   scales at the next 256-byte boundary: [E][U][KG][2][512 B] atoms, U = ceil(R / 128) for
+//          G = 2 (atom pair = gate, up) and U = ceil(R / 256) for G = 1 (atom pair = the two
+//          128-row halves of a 256-row block); row r and block b of an atom at byte
+//          16 (r % 32) + 4 (r / 32) + b, 1.0 (127) for rows or blocks past the matrix.
+__host__ __device__ inline int mx_kg(int K) { return (K + 127) / 128; }
+__host__ __device__ inline int mx_units(int G, int R) { return G == 2 ? (R + 127) / 128 : (R + 255) / 256; }
+__host__ __device__ inline size_t mx_codes_bytes(int G, int E, int R, int K) {
+    return static_cast<size_t>(E) * mx_kg(K) * G * R * 64;
+}
+__host__ __device__ inline size_t mx_sf_offset(int G, int E, int R, int K) {
+    return (mx_codes_bytes(G, E, R, K) + 255) / 256 * 256;
+}
+__host__ __device__ inline size_t mx_blob_bytes(int G, int E, int R, int K) {
+    return mx_sf_offset(G, E, R, K) + static_cast<size_t>(E) * mx_units(G, R) * mx_kg(K) * 1024;
+}
+// bytes per row of an activation scale array: one e8m0 per 32 columns, rows padded to whole
+// groups of four blocks
+__host__ __device__ inline int mx_sf_row(int K) { return mx_kg(K) * 4; }
+
+struct MxArgs {
+    int phase;                    // 0: gate/up + act -> h (split); 1: down -> e (f32 by route id)
+    int act;
+    float limit, alpha;
+    const uint8_t* w;             // phase 0: gate + up blob (G = 2); phase 1: down blob (G = 1)
+    const uint16_t* b0;           // phase 0 gate bias / phase 1 down bias ([E][R] bf16) or nullptr
+    const uint16_t* b1;           // phase 0 up bias or nullptr
+    int R, K, E;                  // rows per expert matrix, reduction length, experts
+    const uint8_t* bq;            // activations, route-list order: two e4m3 planes [2][rows_in][K]
+    const uint8_t* bsf;           // their e8m0 block scales (of the first plane), transposed:
+                                  // word [g][p] holds the scales of blocks 4g..4g+3 of row p
+    int rows_in;                  // T*k
+    uint8_t* hq;                  // phase 0 out: h split into two e4m3 planes [2][rows_in][R]
+    uint8_t* hsf;                 // phase 0 out: scales of h, transposed like bsf
+    float* e_out;                 // phase 1 out: e [T*k][R] by route id
+    const int32_t* off;           // [E+1]
+    const int32_t* perm;          // [T*k]
+    int* status;
+    int max_split;                // > 1: K may be split (needs part/cnt)
+    float* part;                  // split-K partials [max_split][rows_in][2][R] f32
+    int* cnt;                     // split-K group counters (zero before the launch)
+};
+cudaError_t launch_mx_gemm(const MxArgs& a, int num_sms, cudaStream_t s);
+// bf16 rows (route-list order, row p = x[perm[p] / k]; perm nullptr: row p = x[p]) split into two
+// e4m3 planes [2][n][K] and e8m0 block scales, words [mx_sf_row(K) / 4][n] of four blocks
+cudaError_t launch_mx_split_rows(const uint16_t* x, const int32_t* perm, int k, int K, int n,
+                                 uint8_t* q, uint8_t* sf, cudaStream_t s);
+// canonical codes / scales of one matrix (G = 1) or of gate and up (G = 2: codes1/scales1 = up)
+cudaError_t launch_mx_pack(int G, int nmat, int R, int K, const uint8_t* codes0, const uint8_t* scales0,
+                           const uint8_t* codes1, const uint8_t* scales1, uint8_t* blob, cudaStream_t s);
+
 // records the thread's ts_last_error() message (defined in api.cu); returns `status`
 int record_error_code(int status, const char* msg);
 

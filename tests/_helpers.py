@@ -132,11 +132,12 @@ def round16(v, adt):
 # weights times 16-bit activations); the GPU adds them in f32 in blocked chains, so its error is
 # a small multiple of the unit roundoff times the absolute sum.  Measured on GB300 over every
 # sampled h element of the five configurations (the smallest kappa that names each element the
-# GPU rounded differently from the oracle): at most 0.5 on the streaming GEMV path and on the
-# MXFP4 tensor-core path, at most 4 on the tensor-core path with 16-bit weights (its K = 4096
-# reduction runs through 256 chained MMA steps).  The bounds keep a margin of 4x and 2x.
+# GPU rounded differently from the oracle): at most 0.5 on the streaming GEMV path, at most 1 on
+# the tensor-core path over dequantised MXFP4 weights and at most 4 on the tensor-core path with
+# 16-bit weights (its K = 4096 reduction runs through 256 chained MMA steps).  kappa = 2 for the
+# GEMV path and 8 for every tensor-core path keeps a margin of at least 2x.
 KAPPA_GEMV = 2.0
-KAPPA_TC16 = 8.0
+KAPPA_TC = 8.0
 KAPPA = KAPPA_GEMV
 
 
@@ -144,8 +145,9 @@ def kappa_for(cfg, T, path):
     """kappa of the expert path a call takes (the library's automatic choice for path="auto")."""
     tc_fmt = cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"]
     tc_shape = cfg["H"] % 64 == 0 and cfg["I"] % 64 == 0
-    tc = tc_fmt and tc_shape and (path == "gemm" or (path == "auto" and T > 8))
-    return KAPPA_TC16 if (tc and cfg["fmt"] in ("f16", "bf16")) else KAPPA_GEMV
+    mx = cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
+    tc = (path in ("gemm", "gemm_dequant") or (path == "auto" and T > 8)) and (mx or (tc_fmt and tc_shape))
+    return KAPPA_TC if tc else KAPPA_GEMV
 # f32 evaluation of the activation itself (expf / tanhf, a divide, two multiplies), relative
 ACT_REL = 2.0 ** -20
 # non-flip f32 error of an output beside the flips (down projection and combine in f32)

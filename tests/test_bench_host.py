@@ -35,3 +35,21 @@ def test_traffic_record_used_only_while_the_sources_match(tmp_path, monkeypatch)
     rec.write_text(line.replace("common.cuh", "no_such_file.cu") + " src_sha256=00\n")
     assert bench.captured_traffic("k1", "w1") is None
 
+
+def test_both_bench_arms_name_the_same_workload():
+    from mixture_experts_routed_logits_gb300 import synth
+    names = {bench.workload_name(synth.CONFIGS[c], t) for c, t in [(2, 8)] + bench.PER_CONFIG}
+    assert len(names) == 1 + len(bench.PER_CONFIG)
+    assert bench.workload_name(synth.CONFIGS[2], 8) == "gptoss_decode_T8_H2880_E32_k4_mxfp4"
+    assert bench.workload_name(synth.CONFIGS[3], 512) == "gptoss_prefill_T512_H2880_E32_k4_mxfp4_skew"
+    src = open(bench.__file__).read()
+    # the reference arm labels its line with the same function as the measured arm
+    assert src.count("workload_name(c, T)") == 1 and "workload_name(cfg, T)" in src
+
+
+def test_dtype_label_names_the_path_arithmetic():
+    from mixture_experts_routed_logits_gb300 import synth
+    assert "e2m1" in bench.dtype_label(synth.CONFIGS[2], False)
+    assert "mma.sync" in bench.dtype_label(synth.CONFIGS[2], False)
+    assert "tcgen05" in bench.dtype_label(synth.CONFIGS[5], True)
+    assert "int4" in bench.dtype_label(synth.CONFIGS[4], False)

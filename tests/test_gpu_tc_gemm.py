@@ -53,8 +53,15 @@ def _make(cfg, T, shapes):
     return L, to_device(L, "cuda")
 
 
-@pytest.mark.parametrize("case", CASES, ids=_ids)
-def test_tc_gemm_parity(case):
+# MXFP4 cases run on both tensor-core variants: the block-scaled MMA ("gemm": e2m1 weights,
+# activations split into two e4m3 terms) and the f16 MMA over weights dequantised in shared
+# memory ("gemm_dequant")
+PARITY = [pytest.param(c, p, id=_ids(c) + "-" + p)
+          for c in CASES for p in (("gemm", "gemm_dequant") if c[0] in (2, 3) else ("gemm",))]
+
+
+@pytest.mark.parametrize("case,path", PARITY)
+def test_tc_gemm_parity(case, path):
     moe = _moe()
     cfg, T, shapes = case
     L, D = _make(cfg, T, shapes)
@@ -64,7 +71,7 @@ def test_tc_gemm_parity(case):
     ex, sh = gpu_layer(D)
     ws = moe.alloc_workspace(T, c["k"], ex, sh)
     y, y32 = moe.forward(D["x"], ex, torch.from_numpy(oidx).cuda(), torch.from_numpy(ow).cuda(),
-                         want_f32=True, ws=ws, path="gemm")
+                         want_f32=True, ws=ws, path=path)
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
     oex, _ = oracle_layer(L)
@@ -73,7 +80,7 @@ def test_tc_gemm_parity(case):
     rows = slice(None) if toks is None else toks
     # h elements next to a 16-bit rounding boundary (named by the oracle) and what they may move
     allow, _ = flip_allowance(L, oex, None, oracle.adt_bits_to_f64(xb[rows], c["adt"]), oidx[rows],
-                              ow[rows], c["adt"], kappa=kappa_for(c, T, "gemm"), nthreads=NTHREADS)
+                              ow[rows], c["adt"], kappa=kappa_for(c, T, path), nthreads=NTHREADS)
     check_outputs(oracle.adt_bits_to_f64(bits16(y)[rows], c["adt"]), y32.double().cpu().numpy()[rows],
                   oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"],
                   allow=allow)
@@ -128,7 +135,8 @@ def _widen_scales(L, lo, hi, frac, seed):
         s[pick] = torch.randint(lo, hi + 1, (int(pick.sum()),), generator=g).to(torch.uint8)
 
 
-def test_tc_gemm_mxfp4_scales_outside_normal_f16():
+@pytest.mark.parametrize("path", ["gemm", "gemm_dequant"])
+def test_tc_gemm_mxfp4_scales_outside_normal_f16(path):
     # block scales 2^-23 .. 2^1: below 2^-14 the scale itself is not a normal f16 number, yet
     # every scaled e2m1 value still is an exact f16 number, so the result must match the oracle
     moe = _moe()
@@ -141,7 +149,7 @@ def test_tc_gemm_mxfp4_scales_outside_normal_f16():
     ex, _ = gpu_layer(D)
     ws = moe.alloc_workspace(24, c["k"], ex)
     y, y32 = moe.forward(D["x"], ex, torch.from_numpy(oidx).cuda(), torch.from_numpy(ow).cuda(),
-                         want_f32=True, ws=ws, path="gemm")
+                         want_f32=True, ws=ws, path=path)
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
     oex, _ = oracle_layer(L)
@@ -150,9 +158,78 @@ def test_tc_gemm_mxfp4_scales_outside_normal_f16():
                   oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"])
 
 
+def test_block_scaled_path_takes_any_e8m0_scale():
+    # gate/up block scales 2^-27 .. 2^23 (far outside what the f16 dequantisation represents):
+    # the block-scaled MMA applies e8m0 scales in hardware, so the layer matches the oracle
+    moe = _moe()
+    L = synth.make_layer(2, T=24, shapes=dict(H=256, I=192, E=4, k=2), device="cpu")
+    g = torch.Generator().manual_seed(5)
+    for name in ("gate_s", "up_s"):
+        sc = L["experts"][name]
+        pick = torch.rand(sc.shape, generator=g) < 0.1
+        sc[pick] = torch.randint(100, 151, (int(pick.sum()),), generator=g).to(torch.uint8)
+    D = to_device(L, "cuda")
+    c = L["cfg"]
+    xb = bits16(L["x"])
+    _, _, oidx, ow = oracle_route(L, xb)
+    ex, _ = gpu_layer(D)
+    ws = moe.alloc_workspace(24, c["k"], ex)
+    y, y32 = moe.forward(D["x"], ex, torch.from_numpy(oidx).cuda(), torch.from_numpy(ow).cuda(),
+                         want_f32=True, ws=ws, path="gemm")
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
+    oex, _ = oracle_layer(L)
+    oy, oy32, _ = oracle.moe_forward(xb, c["adt"], oex, oidx, ow, nthreads=NTHREADS)
+    allow, _ = flip_allowance(L, oex, None, oracle.adt_bits_to_f64(xb, c["adt"]), oidx, ow, c["adt"],
+                              kappa=kappa_for(c, 24, "gemm"), nthreads=NTHREADS)
+    check_outputs(oracle.adt_bits_to_f64(bits16(y), c["adt"]), y32.double().cpu().numpy(),
+                  oracle.adt_bits_to_f64(oy, c["adt"]), oy32.astype(np.float64), c["adt"], allow=allow)
+
+
+def test_pack_mx_layout():
+    """The tensor-core MXFP4 blob, byte for byte, against the layout built here with numpy: codes
+    [nmat][KG][G][R][64 B] (128 codes of a row per group of 128 columns, gate and up side by side
+    for a pair, zero codes past K), then (at a 256-byte boundary) the e8m0 scales in 512-byte
+    atoms [nmat][U][KG][2][512] (atom pair = gate and up of 128 rows, or the two 128-row halves
+    of 256 rows), row r and block b of an atom at 16*(r%32) + 4*(r/32) + b, 1.0 (127) for rows and
+    blocks past the matrix."""
+    moe = _moe()
+    g = torch.Generator().manual_seed(2)
+    for pair in (False, True):
+        for nmat, R, K in [(3, 96, 320), (2, 2880, 2880), (1, 32, 128), (2, 288, 256)]:
+            G = 2 if pair else 1
+            codes = [torch.randint(0, 256, (nmat, R, K // 2), generator=g, dtype=torch.uint8) for _ in range(G)]
+            scales = [torch.randint(110, 140, (nmat, R, K // 32), generator=g, dtype=torch.uint8) for _ in range(G)]
+            args = (codes[1].cuda(), scales[1].cuda()) if pair else (None, None)
+            blob = moe.pack_mx(codes[0].cuda(), scales[0].cuda(), *args).cpu().numpy()
+            KG = (K + 127) // 128
+            c = np.zeros((nmat, KG, G, R, 64), np.uint8)
+            for m in range(G):
+                cp = np.zeros((nmat, R, KG * 64), np.uint8)
+                cp[:, :, :K // 2] = codes[m].numpy()
+                c[:, :, m] = cp.reshape(nmat, R, KG, 64).transpose(0, 2, 1, 3)
+            assert np.array_equal(blob[:c.size], c.reshape(-1))
+            off = (c.size + 255) // 256 * 256
+            U = (R + 127) // 128 if pair else (R + 255) // 256
+            span = 128 if pair else 256
+            sp = np.full((G, nmat, U * span, KG * 4), 127, np.uint8)
+            for m in range(G):
+                sp[m, :, :R, :K // 32] = scales[m].numpy()
+            atoms = np.empty((nmat, U, KG, 2, 512), np.uint8)
+            for b in range(512):
+                rr, blk = 32 * ((b % 16) // 4) + b // 16, b % 4
+                for m in range(2):
+                    src = sp[m] if pair else sp[0]
+                    rows = np.arange(U) * span + (0 if pair else 128 * m) + rr
+                    atoms[:, :, :, m, b] = src[:, rows][:, :, blk::4][:, :, :KG]
+            assert blob.size == off + atoms.size
+            assert np.array_equal(blob[off:], atoms.reshape(-1))
+
+
 def test_tc_gemm_reports_scales_it_cannot_represent():
-    # a block scale of 2^-27: its scaled e2m1 values are not all f16 numbers; the tensor-core
-    # path must say so through the device status (the GEMV path computes such layers exactly)
+    # a block scale of 2^-27: its scaled e2m1 values are not all f16 numbers; the dequantising
+    # tensor-core path must say so through the device status (the GEMV path and the
+    # block-scaled path compute such layers exactly)
     moe = _moe()
     L = synth.make_layer(2, T=24, shapes=dict(H=256, I=192, E=4, k=2), device="cpu")
     L["experts"]["gate_s"][1, 3, 2] = 100
@@ -162,6 +239,6 @@ def test_tc_gemm_reports_scales_it_cannot_represent():
     idx = torch.tensor([[1, 2]] * 24, dtype=torch.int32, device="cuda")
     w = torch.full((24, 2), 0.5, dtype=torch.float32, device="cuda")
     ws = moe.alloc_workspace(24, c["k"], ex)
-    moe.forward(D["x"], ex, idx, w, ws=ws, path="gemm")
+    moe.forward(D["x"], ex, idx, w, ws=ws, path="gemm_dequant")
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 2
