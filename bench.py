@@ -362,14 +362,19 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # 16-bit weights of the activation type (H, I multiples of 64), else the streaming GEMV
     gemm_ok = H % 64 == 0 and I % 64 == 0 and (cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"])
     mx_ok = cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
-    gemm_path = (gemm_ok or mx_ok) and (args.path in ("gemm", "gemm_dequant") or (args.path == "auto" and T > 8))
+    # decode batches with MXFP4 + bf16 take the block-scaled decode kernels (prep, phase 1,
+    # phase 2 with the combine) on "auto" and "gemm"
+    mxd_path = (mx_ok and T <= 8 and T * k <= 64 and k <= 8 and H <= 4096
+                and args.path in ("auto", "gemm"))
+    gemm_path = mxd_path or ((gemm_ok or mx_ok) and (args.path in ("gemm", "gemm_dequant") or (args.path == "auto" and T > 8)))
     # GEMV decode (T*k <= 512): router, phase 1, phase 2 (+ fused route list and combine);
     # otherwise router, route list, [gather], phase 1, phase 2, combine; + 2 shared-expert GEMVs
     fused_decode = (not gemm_path) and T * k <= 512
     # MXFP4 with bf16 activations takes the block-scaled MMA (activation split + two GEMMs);
     # "gemm_dequant" the f16 MMA over dequantised weights (gather, h conversion)
-    mx_path = gemm_path and cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16" and args.path != "gemm_dequant"
-    n_launch_step = ((3 if fused_decode else 5 + (1 if gemm_path else 0)
+    mx_path = (gemm_path and not mxd_path and cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
+               and args.path != "gemm_dequant")
+    n_launch_step = ((4 if mxd_path else 3 if fused_decode else 5 + (1 if gemm_path else 0)
                       + (1 if gemm_path and cfg["fmt"] == "mxfp4" and not mx_path else 0))
                      + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail else 0))
 
@@ -411,7 +416,9 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # ---- per-phase breakdown: graphs carrying event-record nodes after every launch ----------------
     # event order in a step: 6 router, 0 route list, 1 phase 1, [2 shared phase 1], 3 phase 2,
     # [4 shared phase 2], 5 combine, [7 Gemma sandwich tail]
-    if gemm_path:
+    if mxd_path:   # router, prep, phase 1, [shared phase 1, shared phase 2], phase 2 + combine
+        order = [6, 0, 1] + ([2, 4] if cfg.get("shared_I") else []) + [3]
+    elif gemm_path:
         order = [6, 0, 1, 3, 5]
     else:   # GEMV: routed phase 1, shared phase 1, shared phase 2, routed phase 2 (+ combine)
         order = [6, 0, 1] + ([2, 4] if cfg.get("shared_I") else []) + [3, 5]
@@ -429,6 +436,9 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
             samples[moe.PHASES[j]].append(prev.elapsed_time(phase_ev[j]))
             prev = phase_ev[j]
     phases = {n: statistics.mean(v) for n, v in samples.items()}
+    if mxd_path:   # the decode kernels' first launch splits x (no route list)
+        phases = {("prep_x_split" if n == "route_list" else "experts_phase2_and_combine" if n == "experts_phase2"
+                   else n): v for n, v in phases.items()}
 
     # ---- algorithmic bytes / FLOPs of the dominant kernel (expert phase 1) ---------------------------
     idx_np = layers[0]["idx"].cpu().numpy()
@@ -463,9 +473,12 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
         step_tf = (p1_flop + p2_flop) / (ms_max * 1e-3) / 1e12
     else:
         achieved = p1_bytes / (p1_ms * 1e-3) / 1e9
-        traffic = None if gemm_path else captured_traffic(f"gemv_{fmt}_phase1", wl)
+        traffic = (captured_traffic("mxd_phase1", wl) if mxd_path
+                   else None if gemm_path else captured_traffic(f"gemv_{fmt}_phase1", wl))
         roof = {"bound": "hbm",
-                "kernel": ("experts_phase1 (tcgen05 block-scaled grouped GEMM, MXFP4 gate/up)"
+                "kernel": ("experts_phase1 (tcgen05 block-scaled decode kernel, stream-K, MXFP4 gate/up)"
+                           if mxd_path else
+                           "experts_phase1 (tcgen05 block-scaled grouped GEMM, MXFP4 gate/up)"
                            if mx_path else
                            "experts_phase1 (tcgen05 grouped GEMM over packed MXFP4, gate/up)"
                            if gemm_path else "experts_phase1 (gate/up GEMV)"),
@@ -507,8 +520,10 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
         "step_tflops": None if step_tf is None else {"TFLOPs": step_tf, "frac": step_tf / bf16_sust},
         "step_hbm": {"bytes": step_bytes, "GBps": step_bytes / (ms_max * 1e-3) / 1e9,
                      "frac": step_bytes / (ms_max * 1e-3) / 1e9 / hbm_peak},
-        "dtype": dtype_label(cfg, gemm_path, mx_path), "workload": wl, "cfg": cfg,
-        "path": ("tcgen05 block-scaled grouped GEMM (kind::mxf8f6f4, TMA + TMEM)" if mx_path
+        "dtype": dtype_label(cfg, gemm_path, mx_path or mxd_path), "workload": wl, "cfg": cfg,
+        "path": ("tcgen05 block-scaled decode kernels (kind::mxf8f6f4, stream-K over every SM, TMA + TMEM; "
+                 "prep, gate/up, down + fused combine)" if mxd_path
+                 else "tcgen05 block-scaled grouped GEMM (kind::mxf8f6f4, TMA + TMEM)" if mx_path
                  else "tcgen05 grouped GEMM (TMA + TMEM)" if gemm_path
                  else "gemv (mma.sync m16n8k16 over streamed tiles)"),
     }

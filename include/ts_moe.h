@@ -77,14 +77,18 @@ typedef enum { TS_ACT_SILU_GLU = 0, TS_ACT_GELU_TANH_GLU = 1, TS_ACT_GPTOSS_SWIG
 
 /* Path selection for ts_moe_forward_path. */
 typedef enum {
-    TS_PATH_AUTO = 0,  /* GEMV path for T <= 8 tokens, else the tensor-core grouped GEMM when the
-                          format has one (MXFP4, or f16/bf16 weights of the activation type)
-                          and H, I are multiples of 64, else the GEMV path                      */
+    TS_PATH_AUTO = 0,  /* T <= 8 tokens: the block-scaled decode kernels when they apply (MXFP4
+                          with its tensor-core blobs, bf16 activations, T*k <= 64, k <= 8,
+                          H <= 4096), else the GEMV path.  T > 8: the tensor-core grouped GEMM
+                          when the format has one (MXFP4, or f16/bf16 weights of the activation
+                          type) and H, I are multiples of 64, else the GEMV path              */
     TS_PATH_GEMV = 1,  /* streaming GEMV kernels (any T)                                        */
     TS_PATH_GEMM = 2,  /* tcgen05 grouped GEMM.  MXFP4 weights with bf16 activations and the
                           tensor-core blobs present (gateup_mx/down_mx): block-scaled MMA
                           (kind::mxf8f6f4, e2m1 x e4m3 with e8m0 scales; activations split
-                          exactly into two e4m3 terms).  Otherwise as TS_PATH_GEMM_DEQUANT      */
+                          exactly into two e4m3 terms), through the decode kernels (prep, gate/up,
+                          down + combine; stream-K over every SM) when T <= 8 and they apply.
+                          Otherwise as TS_PATH_GEMM_DEQUANT                                    */
     TS_PATH_GEMM_DEQUANT = 3  /* tcgen05 grouped GEMM on 16-bit operands: 16-bit weights of the
                           activation type as they are; MXFP4 weights dequantised to f16 in
                           shared memory, exact for e8m0 scales 2^-23..2^13 (a block outside
@@ -316,12 +320,12 @@ ts_status ts_moe_device_status(void* ws, int32_t* code, void* stream);
 
 /* Exercises the bounded waits (test use; the pages' counterpart is the refusal convention:
  * fail with a status, never hang or degrade).  mode 1: the next ts_moe_forward* call on this
- * thread that runs the streaming GEMV expert path withholds the first weight copy of its
- * phase-1 launch, so that launch's consumer warps wait on a copy that never arrives; their
- * bounded wait (about 2^31 SM clocks, a second) runs out, they report TS_ERR_TIMEOUT through
- * the device status word (ts_moe_device_status), the launch drains the copies it did issue and
- * returns, and the call's outputs are meaningless.  The setting is consumed by the next
- * forward call whichever path it takes.  mode 0 clears it.                                  */
+ * thread that runs the streaming GEMV expert path or the block-scaled decode kernels withholds
+ * the first weight copy of its phase-1 launch, so that launch's consumer warps wait on a copy
+ * that never arrives; their bounded wait (about 2^31 SM clocks, a second) runs out, they
+ * report TS_ERR_TIMEOUT through the device status word (ts_moe_device_status), the launch
+ * drains the copies it did issue and returns, and the call's outputs are meaningless.  The
+ * setting is consumed by the next forward call whichever path it takes.  mode 0 clears it.  */
 ts_status ts_moe_set_wait_test(int32_t mode);
 
 /* Per-phase timing (the counterpart of the pages' PhaseCounters / per-command-buffer GPU

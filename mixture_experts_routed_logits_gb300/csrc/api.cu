@@ -98,6 +98,7 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
 struct WsLayout {
     size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hinv, h16, cmb, part, tcnt, total;
     size_t xq, xsf, hq, hsf;   // block-scaled path: split activations and their scales
+    size_t dxs, dhs, dpart, dcnt, dcnt_bytes;   // block-scaled decode kernels (T <= 8)
     size_t tcnt_n;        // split-K group counters per phase
     int max_split;        // > 1 when the partials fit (decode sizes)
 };
@@ -134,6 +135,17 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
         L.xsf = take(Tk * mx_sf_row(ex->H));
         L.hq = take(2 * Tk * ex->I);
         L.hsf = take(Tk * mx_sf_row(ex->I));
+        if (T <= kMxdTokens && Tk <= kMxdMaxTouched && k <= kMxdMaxK && ex->H <= kMxdMaxH) {
+            // decode kernels: the split x and h images, stream-K partials, and the part /
+            // row-block counters
+            const size_t nt = static_cast<size_t>(ex->E) < Tk ? static_cast<size_t>(ex->E) : Tk;
+            const size_t mb0 = (static_cast<size_t>(ex->I) + 127) / 128, mb1 = (static_cast<size_t>(ex->H) + 255) / 256;
+            L.dxs = take(((static_cast<size_t>(ex->H) + 127) / 128) * kMxdBStage + 512);
+            L.dhs = take(nt * mb0 * kMxdHImage);
+            L.dpart = take(static_cast<size_t>(kMxdMaxCtas) * 2 * 2 * 128 * 8 * 4);
+            L.dcnt_bytes = round_up((nt * (mb0 > mb1 ? mb0 : mb1) * 4 + mb1 * 4) * 4, 256);
+            L.dcnt = take(L.dcnt_bytes);
+        }
     }
     // split-K partials of the tensor-core path for decode-sized calls (few routes, so the few
     // (expert, row block) tiles are cut along K to reach every SM): [part][route][2][rows] f32
@@ -150,11 +162,117 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
     return L;
 }
 
+// Decode batches (T <= 8) with MXFP4 blobs and bf16 activations: block-scaled phase 1 (route
+// tables, gate/up, activation -> h per touched expert), the shared expert if any, block-scaled
+// phase 2 (down -> e, slot-ordered combine -> y).
+ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int32_t* idx,
+                      const float* w, int k, const ts_moe_experts* shared, void* y, float* y_f32,
+                      unsigned char* W, const WsLayout& L, cudaStream_t st);
+
 ts_status launch_gemv_checked(const GemvArgs& a, cudaStream_t st, const char* what) {
     const int sms = num_sms_current();
     if (sms <= 0) return fail(TS_ERR_CUDA, "%s: no CUDA device", what);
     cudaError_t e = launch_gemv(a, sms, st);
     if (e != cudaSuccess) return cuda_fail(e, what);
+    return TS_OK;
+}
+
+ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int32_t* idx,
+                      const float* w, int k, const ts_moe_experts* shared, void* y, float* y_f32,
+                      unsigned char* W, const WsLayout& L, cudaStream_t st) {
+    const int sms = num_sms_current();
+    if (sms <= 0) return fail(TS_ERR_CUDA, "ts_moe_forward: no CUDA device");
+    int* status = reinterpret_cast<int*>(W + L.status);
+    int* cnt = reinterpret_cast<int*>(W + L.dcnt);
+    const int nt_max = ex->E < T * k ? ex->E : T * k;
+    const int mb0 = (ex->I + 127) / 128, mb1 = (ex->H + 255) / 256;
+    MxdArgs M{};
+    M.phase = 0;
+    M.act = ex->act;
+    M.limit = ex->swiglu_limit;
+    M.alpha = ex->swiglu_alpha;
+    M.w = static_cast<const uint8_t*>(ex->gateup_mx);
+    M.b0 = static_cast<const uint16_t*>(ex->gate_b);
+    M.b1 = static_cast<const uint16_t*>(ex->up_b);
+    M.R = ex->I;
+    M.K = ex->H;
+    M.E = ex->E;
+    M.T = T;
+    M.k = k;
+    M.idx = idx;
+    M.wr = w;
+    M.x = static_cast<const uint16_t*>(x);
+    M.xs = W + L.dxs;
+    M.hs = W + L.dhs;
+    M.part = reinterpret_cast<float*>(W + L.dpart);
+    // part counters (shared by both phases), then phase 2's row-block counters: the prep kernel
+    // zeroes them (the kernels leave them zero; this covers a call that stopped early)
+    M.tcnt = cnt;
+    M.ncnt = static_cast<int>(L.dcnt_bytes / 4);
+    M.status = status;
+    M.stall = g_wait_test;
+    g_wait_test = 0;
+    cudaError_t e = launch_mxd_prep(M, st);
+    if (e == cudaSuccess) e = phase_mark(0, st);
+    if (e == cudaSuccess) e = launch_mxd(M, sms, st);
+    if (e == cudaSuccess) e = phase_mark(1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled decode phase 1");
+    if (shared) {
+        GemvArgs gs{};
+        gs.fmt = shared->fmt;
+        gs.act = shared->act;
+        gs.limit = shared->swiglu_limit;
+        gs.alpha = shared->swiglu_alpha;
+        gs.adt = TS_DT_BF16;
+        gs.T = T;
+        gs.k = 1;
+        gs.E = 1;
+        gs.status = status;
+        gs.phase = 0;
+        gs.w0 = static_cast<const uint8_t*>(shared->gate);
+        gs.w1 = static_cast<const uint8_t*>(shared->up);
+        gs.b0 = static_cast<const uint16_t*>(shared->gate_b);
+        gs.b1 = static_cast<const uint16_t*>(shared->up_b);
+        gs.R = shared->I;
+        gs.K = shared->H;
+        gs.mat_bytes = matrix_bytes(shared->fmt, shared->I, shared->H);
+        gs.in = static_cast<const uint16_t*>(x);
+        gs.out = W + L.hs;
+        gs.dense = 1;
+        ts_status s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 1");
+        if (s != TS_OK) return s;
+        if ((e = phase_mark(2, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
+        gs.phase = 1;
+        gs.w0 = static_cast<const uint8_t*>(shared->down);
+        gs.w1 = nullptr;
+        gs.b0 = static_cast<const uint16_t*>(shared->down_b);
+        gs.b1 = nullptr;
+        gs.R = shared->H;
+        gs.K = shared->I;
+        gs.mat_bytes = matrix_bytes(shared->fmt, shared->H, shared->I);
+        gs.in = reinterpret_cast<const uint16_t*>(W + L.hs);
+        gs.out = W + L.s;
+        if ((s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 2")) != TS_OK) return s;
+        if ((e = phase_mark(4, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
+    }
+    M.phase = 1;
+    M.stall = 0;
+    M.w = static_cast<const uint8_t*>(ex->down_mx);
+    M.b0 = static_cast<const uint16_t*>(ex->down_b);
+    M.b1 = nullptr;
+    M.R = ex->H;
+    M.K = ex->I;
+    M.x = nullptr;
+    M.e_out = reinterpret_cast<float*>(W + L.e);
+    M.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
+    M.y = y;
+    M.y_f32 = y_f32;
+    // phase 1 left every part counter at zero again; phase 2 reuses them
+    M.rbcnt = cnt + static_cast<size_t>(nt_max) * (mb0 > mb1 ? mb0 : mb1) * 4;
+    e = launch_mxd(M, sms, st);
+    if (e == cudaSuccess) e = phase_mark(3, st);
+    if (e == cudaSuccess) e = phase_mark(5, st);
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled decode phase 2");
     return TS_OK;
 }
 
@@ -319,6 +437,8 @@ size_t ts_moe_workspace_size(int32_t T, int32_t k, const ts_moe_experts* ex,
     size_t need = ws_layout(T, k, ex, shared).total;
     const int tsplit = 64 / k;
     if (T > tsplit && tsplit > 0) need = std::max(need, ws_layout(tsplit, k, ex, shared).total);
+    const int tdec = std::min(tsplit, static_cast<int>(kMxdTokens));   // block-scaled decode kernels
+    if (T > tdec && tdec > 0) need = std::max(need, ws_layout(tdec, k, ex, shared).total);
     return need;
 }
 
@@ -364,6 +484,9 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
                     "activation type, with H %% 64 == 0 and I %% 64 == 0 (or MXFP4 with its "
                     "tensor-core blobs and bf16 activations) (fmt=%d adt=%d H=%d I=%d)",
                     what, ex->fmt, adt, ex->H, ex->I);
+    // decode batches (T <= 8, their workspace regions present) take the block-scaled decode
+    // kernels (route tables built inside, combine fused into the last) on "gemm" and "auto"
+    const bool use_mxd = mx_ok && L.dcnt_bytes > 0 && (path == TS_PATH_GEMM || path == TS_PATH_AUTO);
     const bool use_mx = mx_ok && (path == TS_PATH_GEMM || (path == TS_PATH_AUTO && T > 8));
     const bool use_gemm = use_mx || path == TS_PATH_GEMM || path == TS_PATH_GEMM_DEQUANT ||
                           (path == TS_PATH_AUTO && T > 8 && (gemm_fmt || quant_gemm) && gemm_shape);
@@ -375,6 +498,7 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     int32_t* inv = reinterpret_cast<int32_t*>(W + L.inv);
 
     cudaError_t e = cudaSuccess;
+    if (use_mxd) return forward_mxd(x, T, ex, idx, w, k, shared, y, y_f32, W, L, st);
     if (use_gemm || static_cast<long long>(T) * k > 512)   // else built inside the GEMV kernels
         e = launch_build_routes(idx, T, ex->E, k, off, perm, inv, status, st);
     if (e == cudaSuccess) e = phase_mark(0, st);

@@ -2,8 +2,9 @@
 host reads, the call returns normally and the CUDA context stays usable.
 
 The wait is made to run out without any GPU fault: ts_moe_set_wait_test makes the next call's
-phase-1 GEMV launch withhold its first weight copy (a copy nothing else will issue), so the
-consumer warps' bounded wait on it expires after about a second.  The pages' convention is to
+phase-1 launch (the streaming GEMV, or the block-scaled decode kernel) withhold its first weight
+copy (a copy nothing else will issue), so the consumer warps' bounded wait on it expires after
+about a second.  The pages' convention is to
 fail with a status rather than hang or quietly degrade (Gemma-4 batched routed prefill,
 src/families/gemma4/moe_batch.rs, RealForwardError::Unsupported refusals)."""
 import numpy as np
@@ -22,23 +23,25 @@ def _built():
     __graft_entry__.build()
 
 
-def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable():
+@pytest.mark.parametrize("path", ["gemv", "auto"])
+def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable(path):
+    """path "auto" at T = 8 with MXFP4 blobs runs the block-scaled decode kernels."""
     import mixture_experts_routed_logits_gb300 as moe
     L = to_device(synth.make_layer(2, T=8, shapes=dict(H=512, I=384, E=8, k=4), device="cpu"), "cuda")
     c = L["cfg"]
     ex, _ = gpu_layer(L)
     idx, w, _, _ = moe.router_route(L["x"], L["Wr"], c["k"], router_bias=L["router_bias"])
     ws = moe.alloc_workspace(8, c["k"], ex)
-    ref, ref32 = (t.clone() for t in moe.forward(L["x"], ex, idx, w, ws=ws, want_f32=True))
+    ref, ref32 = (t.clone() for t in moe.forward(L["x"], ex, idx, w, ws=ws, want_f32=True, path=path))
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
     moe.set_wait_test(1)
-    moe.forward(L["x"], ex, idx, w, ws=ws)          # returns TS_OK: the failure is on the device
+    moe.forward(L["x"], ex, idx, w, ws=ws, path=path)   # returns TS_OK: the failure is on the device
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 4               # TS_ERR_TIMEOUT
     assert moe.device_status(ws) == 0               # read and cleared
     # the setting was consumed and the context is usable: the next call is the first one again
-    y, y32 = moe.forward(L["x"], ex, idx, w, ws=ws, want_f32=True)
+    y, y32 = moe.forward(L["x"], ex, idx, w, ws=ws, want_f32=True, path=path)
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
     assert torch.equal(y.view(torch.int16), ref.view(torch.int16))

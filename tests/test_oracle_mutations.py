@@ -16,7 +16,8 @@ MUTATIONS = {
     "combine drops routing weight": ("float p = ws * eo[j];", "float p = eo[j];"),
     "gelu constant": ("0.044715 * g * g * g", "0.04471 * g * g * g"),
     "bias not before top-k": ("key[e] = bias ? l[e] + bias[e] : l[e];", "key[e] = l[e];"),
-    "up bias dropped": ("if (X->up_b) u +=", "if (0) u +="),
+    "up bias dropped": ("if (X->up_b) u += or_bf16_to_double(X->up_b[(size_t)e * I + i]);\n        double h",
+                        "if (0) u += or_bf16_to_double(X->up_b[(size_t)e * I + i]);\n        double h"),
     "swiglu lower clamp sign": ("if (u < -L) u = -L;", "if (u < -L) u = L;"),
     "int4 min dropped": ("return (double)q * scale + mn;", "return (double)q * scale;"),
     "e8m0 bias": ("return ldexp(1.0, byte - 127);", "return ldexp(1.0, byte - 128);"),
