@@ -362,10 +362,10 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # 16-bit weights of the activation type (H, I multiples of 64), else the streaming GEMV
     gemm_ok = H % 64 == 0 and I % 64 == 0 and (cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"])
     mx_ok = cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
-    # decode batches with MXFP4 + bf16 take the block-scaled decode kernels (prep, phase 1,
-    # phase 2 with the combine) on "auto" and "gemm"
+    # decode batches with MXFP4 + bf16 take the block-scaled decode kernels (prep, then one
+    # launch for both phases and the combine) on "gemm", and on "auto" from 3 tokens
     mxd_path = (mx_ok and T <= 8 and T * k <= 64 and k <= 8 and H <= 4096
-                and args.path in ("auto", "gemm"))
+                and (args.path == "gemm" or (args.path == "auto" and T >= 3)))
     gemm_path = mxd_path or ((gemm_ok or mx_ok) and (args.path in ("gemm", "gemm_dequant") or (args.path == "auto" and T > 8)))
     # GEMV decode (T*k <= 512): router, phase 1, phase 2 (+ fused route list and combine);
     # otherwise router, route list, [gather], phase 1, phase 2, combine; + 2 shared-expert GEMVs
@@ -374,7 +374,7 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # "gemm_dequant" the f16 MMA over dequantised weights (gather, h conversion)
     mx_path = (gemm_path and not mxd_path and cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
                and args.path != "gemm_dequant")
-    n_launch_step = ((4 if mxd_path else 3 if fused_decode else 5 + (1 if gemm_path else 0)
+    n_launch_step = ((3 if mxd_path else 3 if fused_decode else 5 + (1 if gemm_path else 0)
                       + (1 if gemm_path and cfg["fmt"] == "mxfp4" and not mx_path else 0))
                      + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail else 0))
 
@@ -416,8 +416,8 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # ---- per-phase breakdown: graphs carrying event-record nodes after every launch ----------------
     # event order in a step: 6 router, 0 route list, 1 phase 1, [2 shared phase 1], 3 phase 2,
     # [4 shared phase 2], 5 combine, [7 Gemma sandwich tail]
-    if mxd_path:   # router, prep, phase 1, [shared phase 1, shared phase 2], phase 2 + combine
-        order = [6, 0, 1] + ([2, 4] if cfg.get("shared_I") else []) + [3]
+    if mxd_path:   # router, prep, [shared phase 1, shared phase 2], both phases + combine
+        order = [6, 0] + ([2, 4] if cfg.get("shared_I") else []) + [1]
     elif gemm_path:
         order = [6, 0, 1, 3, 5]
     else:   # GEMV: routed phase 1, shared phase 1, shared phase 2, routed phase 2 (+ combine)
@@ -436,8 +436,8 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
             samples[moe.PHASES[j]].append(prev.elapsed_time(phase_ev[j]))
             prev = phase_ev[j]
     phases = {n: statistics.mean(v) for n, v in samples.items()}
-    if mxd_path:   # the decode kernels' first launch splits x (no route list)
-        phases = {("prep_x_split" if n == "route_list" else "experts_phase2_and_combine" if n == "experts_phase2"
+    if mxd_path:   # the prep launch splits x (no route list); one launch runs both phases
+        phases = {("prep_x_split" if n == "route_list" else "experts_fused" if n == "experts_phase1"
                    else n): v for n, v in phases.items()}
 
     # ---- algorithmic bytes / FLOPs of the dominant kernel (expert phase 1) ---------------------------
@@ -457,7 +457,7 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     if cfg.get("shared_I"):
         shared_bytes = 3 * H * cfg["shared_I"] * 2
     step_bytes = p1_bytes + p2_bytes + shared_bytes + E * H * 2 + T * H * 2 * 2 + T * k * H * 4
-    p1_ms = phases["experts_phase1"]
+    p1_ms = phases["experts_fused" if mxd_path else "experts_phase1"]
     routes = T * k
     p1_flop = 2.0 * routes * 2 * I * H
     p2_flop = 2.0 * routes * H * I
@@ -472,19 +472,21 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
                 "traffic": None, "algorithmic_flop": p1_flop, "launch_ms": p1_ms}
         step_tf = (p1_flop + p2_flop) / (ms_max * 1e-3) / 1e12
     else:
-        achieved = p1_bytes / (p1_ms * 1e-3) / 1e9
-        traffic = (captured_traffic("mxd_phase1", wl) if mxd_path
+        # the decode kernels run both phases in one launch: its bytes are both phases'
+        k_bytes = p1_bytes + p2_bytes if mxd_path else p1_bytes
+        achieved = k_bytes / (p1_ms * 1e-3) / 1e9
+        traffic = (captured_traffic("mxd_fused", wl) if mxd_path
                    else None if gemm_path else captured_traffic(f"gemv_{fmt}_phase1", wl))
         roof = {"bound": "hbm",
-                "kernel": ("experts_phase1 (tcgen05 block-scaled decode kernel, stream-K, MXFP4 gate/up)"
-                           if mxd_path else
+                "kernel": ("experts_fused (tcgen05 block-scaled decode kernel: gate/up, down, combine; "
+                           "stream-K, cooperative)" if mxd_path else
                            "experts_phase1 (tcgen05 block-scaled grouped GEMM, MXFP4 gate/up)"
                            if mx_path else
                            "experts_phase1 (tcgen05 grouped GEMM over packed MXFP4, gate/up)"
                            if gemm_path else "experts_phase1 (gate/up GEMV)"),
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_source": peak_src,
-                "traffic": traffic, "algorithmic_bytes": p1_bytes, "launch_ms": p1_ms}
+                "traffic": traffic, "algorithmic_bytes": k_bytes, "launch_ms": p1_ms}
         step_tf = None
 
     # ---- end to end through the public API with host buffers ---------------------------------------

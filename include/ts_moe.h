@@ -77,9 +77,10 @@ typedef enum { TS_ACT_SILU_GLU = 0, TS_ACT_GELU_TANH_GLU = 1, TS_ACT_GPTOSS_SWIG
 
 /* Path selection for ts_moe_forward_path. */
 typedef enum {
-    TS_PATH_AUTO = 0,  /* T <= 8 tokens: the block-scaled decode kernels when they apply (MXFP4
-                          with its tensor-core blobs, bf16 activations, T*k <= 64, k <= 8,
-                          H <= 4096), else the GEMV path.  T > 8: the tensor-core grouped GEMM
+    TS_PATH_AUTO = 0,  /* 3 <= T <= 8 tokens: the block-scaled decode kernels when they apply
+                          (MXFP4 with its tensor-core blobs, bf16 activations, T*k <= 64,
+                          k <= 8, H <= 4096), else (and for T <= 2) the GEMV path.  T > 8: the
+                          tensor-core grouped GEMM
                           when the format has one (MXFP4, or f16/bf16 weights of the activation
                           type) and H, I are multiples of 64, else the GEMV path              */
     TS_PATH_GEMV = 1,  /* streaming GEMV kernels (any T)                                        */

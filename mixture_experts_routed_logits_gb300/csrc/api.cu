@@ -142,8 +142,8 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
             const size_t mb0 = (static_cast<size_t>(ex->I) + 127) / 128, mb1 = (static_cast<size_t>(ex->H) + 255) / 256;
             L.dxs = take(((static_cast<size_t>(ex->H) + 127) / 128) * kMxdBStage + 512);
             L.dhs = take(nt * mb0 * kMxdHImage);
-            L.dpart = take(static_cast<size_t>(kMxdMaxCtas) * 2 * 2 * 128 * 8 * 4);
-            L.dcnt_bytes = round_up((nt * (mb0 > mb1 ? mb0 : mb1) * 4 + mb1 * 4) * 4, 256);
+            L.dpart = take(static_cast<size_t>(kMxdMaxCtas) * 2 * 2 * kMxdPartFloats * 4);
+            L.dcnt_bytes = round_up((nt + nt * mb0 * 4 + nt * mb1 * 4 + mb1 * 4) * 4, 256);
             L.dcnt = take(L.dcnt_bytes);
         }
     }
@@ -183,19 +183,17 @@ ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int3
     const int sms = num_sms_current();
     if (sms <= 0) return fail(TS_ERR_CUDA, "ts_moe_forward: no CUDA device");
     int* status = reinterpret_cast<int*>(W + L.status);
-    int* cnt = reinterpret_cast<int*>(W + L.dcnt);
-    const int nt_max = ex->E < T * k ? ex->E : T * k;
-    const int mb0 = (ex->I + 127) / 128, mb1 = (ex->H + 255) / 256;
     MxdArgs M{};
-    M.phase = 0;
     M.act = ex->act;
     M.limit = ex->swiglu_limit;
     M.alpha = ex->swiglu_alpha;
-    M.w = static_cast<const uint8_t*>(ex->gateup_mx);
-    M.b0 = static_cast<const uint16_t*>(ex->gate_b);
-    M.b1 = static_cast<const uint16_t*>(ex->up_b);
-    M.R = ex->I;
-    M.K = ex->H;
+    M.wgu = static_cast<const uint8_t*>(ex->gateup_mx);
+    M.wd = static_cast<const uint8_t*>(ex->down_mx);
+    M.bg = static_cast<const uint16_t*>(ex->gate_b);
+    M.bu = static_cast<const uint16_t*>(ex->up_b);
+    M.bd = static_cast<const uint16_t*>(ex->down_b);
+    M.H = ex->H;
+    M.I = ex->I;
     M.E = ex->E;
     M.T = T;
     M.k = k;
@@ -204,20 +202,24 @@ ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int3
     M.x = static_cast<const uint16_t*>(x);
     M.xs = W + L.dxs;
     M.hs = W + L.dhs;
+    M.e_out = reinterpret_cast<float*>(W + L.e);
+    M.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
+    M.y = y;
+    M.y_f32 = y_f32;
     M.part = reinterpret_cast<float*>(W + L.dpart);
-    // part counters (shared by both phases), then phase 2's row-block counters: the prep kernel
-    // zeroes them (the kernels leave them zero; this covers a call that stopped early)
-    M.tcnt = cnt;
+    // the counters (h slices per touched expert, parts per tile of each phase, finished tiles
+    // per row block of phase 2): the prep kernel zeroes them (the kernels leave them zero; this
+    // covers a call that stopped early)
+    M.cnt = reinterpret_cast<int*>(W + L.dcnt);
     M.ncnt = static_cast<int>(L.dcnt_bytes / 4);
     M.status = status;
     M.stall = g_wait_test;
     g_wait_test = 0;
     cudaError_t e = launch_mxd_prep(M, st);
     if (e == cudaSuccess) e = phase_mark(0, st);
-    if (e == cudaSuccess) e = launch_mxd(M, sms, st);
-    if (e == cudaSuccess) e = phase_mark(1, st);
-    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled decode phase 1");
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled decode prep");
     if (shared) {
+        // the shared expert's output seeds the combine of the fused launch
         GemvArgs gs{};
         gs.fmt = shared->fmt;
         gs.act = shared->act;
@@ -255,24 +257,11 @@ ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int3
         if ((s = launch_gemv_checked(gs, st, "ts_moe_forward: shared expert phase 2")) != TS_OK) return s;
         if ((e = phase_mark(4, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
     }
-    M.phase = 1;
-    M.stall = 0;
-    M.w = static_cast<const uint8_t*>(ex->down_mx);
-    M.b0 = static_cast<const uint16_t*>(ex->down_b);
-    M.b1 = nullptr;
-    M.R = ex->H;
-    M.K = ex->I;
-    M.x = nullptr;
-    M.e_out = reinterpret_cast<float*>(W + L.e);
-    M.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
-    M.y = y;
-    M.y_f32 = y_f32;
-    // phase 1 left every part counter at zero again; phase 2 reuses them
-    M.rbcnt = cnt + static_cast<size_t>(nt_max) * (mb0 > mb1 ? mb0 : mb1) * 4;
     e = launch_mxd(M, sms, st);
+    if (e == cudaSuccess) e = phase_mark(1, st);
     if (e == cudaSuccess) e = phase_mark(3, st);
     if (e == cudaSuccess) e = phase_mark(5, st);
-    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled decode phase 2");
+    if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled decode kernel");
     return TS_OK;
 }
 
@@ -485,8 +474,11 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
                     "tensor-core blobs and bf16 activations) (fmt=%d adt=%d H=%d I=%d)",
                     what, ex->fmt, adt, ex->H, ex->I);
     // decode batches (T <= 8, their workspace regions present) take the block-scaled decode
-    // kernels (route tables built inside, combine fused into the last) on "gemm" and "auto"
-    const bool use_mxd = mx_ok && L.dcnt_bytes > 0 && (path == TS_PATH_GEMM || path == TS_PATH_AUTO);
+    // kernels (route tables built inside, combine fused into the last) on "gemm", and on "auto"
+    // from 3 tokens (measured on GB300 with the router in front: the streaming GEMV is faster at
+    // T = 1, level at T = 2, slower from T = 4)
+    const bool use_mxd = mx_ok && L.dcnt_bytes > 0 &&
+                         (path == TS_PATH_GEMM || (path == TS_PATH_AUTO && T >= kMxdAutoMinT));
     const bool use_mx = mx_ok && (path == TS_PATH_GEMM || (path == TS_PATH_AUTO && T > 8));
     const bool use_gemm = use_mx || path == TS_PATH_GEMM || path == TS_PATH_GEMM_DEQUANT ||
                           (path == TS_PATH_AUTO && T > 8 && (gemm_fmt || quant_gemm) && gemm_shape);

@@ -1,12 +1,13 @@
 // gemm_mxd.cu -- steps 3-5 of the routed-expert layer for decode batches (T <= 8 tokens) with
-// MXFP4 experts and bf16 activations, on the block-scaled tensor cores, in three launches:
-//   prep:    the T token rows split into two e4m3 terms (one e8m0 scale per row), written once
-//            as the shared-memory image of B that phase 1 copies; the counters zeroed;
-//   phase 1: the route tables from idx, gate and up of every touched expert streamed once, bias
-//            + activation, h split into two e4m3 terms (one e8m0 scale per 32 values) and
-//            written as the B image of phase 2's K stage;
-//   phase 2: down of every touched expert streamed once, bias, e per route, and the slot-ordered
-//            combine into y by the CTA that finishes a row block last.
+// MXFP4 experts and bf16 activations, on the block-scaled tensor cores, in two launches:
+//   prep:  the T token rows split into two e4m3 terms (one e8m0 scale per row), written once
+//          as the shared-memory image of B's K stages; the counters zeroed;
+//   fused: one persistent cooperative launch (one CTA per SM) running
+//          phase 1 -- the route tables from idx, gate and up of every touched expert streamed
+//            once, bias + activation, h split into two e4m3 terms (one e8m0 scale per 32 values)
+//            and written as the B image of phase 2's K stage, and
+//          phase 2 -- down of every touched expert streamed once, bias, e per route, and the
+//            slot-ordered combine into y by the CTA that finishes a row block last.
 //
 // Source pages (docs.rs, turbospark-runtime 0.3.0):
 //   gpt-oss routed-expert pass (src/families/gptoss/moe.rs): the decode pair of encoders (phase 1
@@ -14,7 +15,7 @@
 //     reduction (router rank, slot-index order), the zero residual seed.
 //   Gemma-4 batched routed prefill (src/families/gemma4/moe_batch.rs): the route list.
 //
-// Design (GB300, one CTA per SM, persistent):
+// Design (GB300):
 //   * Every CTA builds the route tables itself from idx (T*k <= 64 entries): the touched experts in
 //     ascending order and, per (touched expert, token), the route id or none.  No route-list
 //     launch.
@@ -26,18 +27,26 @@
 //     which lets the CTA that finishes a 128-row tile of phase 1 split it on the spot: the tile
 //     is exactly one 128-column K stage of phase 2.  Each stage's 2 KB of B rows is copied into
 //     the ring slot beside the weights (from L2).
+//   * Stream-K, per phase: the work units (touched expert, block of weight rows, K stage) are cut
+//     into equal contiguous ranges, one per CTA; a tile split between CTAs parks its partial
+//     sums and the CTA that brings the last part finishes it, summing the parts in K (= CTA)
+//     order, so results are deterministic.  A CTA takes its phase-1 segments, then its phase-2
+//     ones, each list in the order first, last, middle (the first and last may share their tile
+//     with a neighbour, so their parts meet early).
+//   * The two phases meet through one counter per touched expert: each finished phase-1 tile adds
+//     one per 32-row slice after writing its h image (release); phase 2's activation producer
+//     waits (acquire, bounded) until its expert's count is complete before copying that expert's
+//     h stages.  The weight producer never waits on it, so phase 2's down weights stream in while
+//     the last phase-1 tiles finish.  The launch is cooperative: every CTA is resident, so the
+//     wait always ends.
 //   * The weights stream from HBM through a ring of 6 slots; a 4-bit code takes a byte in
 //     shared memory in the block-scaled MMA's operand layout, so shared memory caps the bytes in
 //     flight (about 96 KB of HBM data per SM).  An L2 prefetch ahead of the ring was measured
 //     slower (its copies compete with the ring's at the start and cost the producer an
 //     instruction per stage), so there is none.
-//   * Stream-K: the work units (touched expert, block of weight rows, K stage) are cut into
-//     equal contiguous ranges, one per CTA; a tile split between CTAs parks its partial sums and
-//     the CTA that brings the last part finishes it, summing the parts in K (= CTA) order, so
-//     results are deterministic.
 //   * Warps: 0 weight producer (one 16 KB tensor copy per stage), 7 scale and activation producer
-//     (bulk copies), 6 scale copies into TMEM, 1 MMA issuer, 2-5 epilogue.
-//     Every mbarrier wait is bounded.
+//     (bulk copies), 6 scale copies into TMEM, 1 MMA issuer, 2-5 epilogue.  Every wait is
+//     bounded.
 #include "mx_common.cuh"
 
 namespace tsmoe {
@@ -55,32 +64,76 @@ constexpr uint32_t kDColSf = 80;       // scales of slot s at 80 + 16 s (A: 8 co
 struct MxdLayout {
     int nslot, slot_bytes, sfa_off, b_off;   // ring slot: A codes 32 KB, scale atoms 1 KB, B stage
                                              // 2 KB (phase 2: + its scale atom 512 B)
-    int sfb_off;                             // phase 1: x scale atom (512 B)
+    int sfb_off;                             // x scale atom (512 B)
     int tail_off;
 };
 
 struct MxdParams {
-    CUtensorMap tmA;
+    CUtensorMap tmA[2];                      // codes of gate + up (phase 1), down (phase 2)
     MxdArgs a;
     MxdLayout ly;
 };
 
 struct MxdTail {
-    uint64_t full[kDMaxSlots];      // weight codes, scale atoms and the B stage landed
+    uint64_t full[kDMaxSlots];      // the slot's weight codes, scale atoms and B stage landed
     uint64_t sfull[kDMaxSlots];     // the slot's scales copied into TMEM
     uint64_t empty[kDMaxSlots];     // the slot's MMAs done
     uint64_t tfull[2];
     uint64_t tempty[2];
-    uint64_t bready;                // phase 1: the x scale atom landed
+    uint64_t bready;                // the x scale atom landed
     uint32_t tmem_base;
     volatile int abort_flag;
+    volatile int w0_issued;         // stages the weight producer has issued
+    volatile int w0_done;           // the weight producer has left its loop
     int nt;
     int touched[kMxdMaxTouched];
     int rid[kMxdMaxTouched][kMxdTokens];
-    float wr[kMxdTokens * kMxdMaxK];  // phase 2: routing weights [t][s]
+    float wr[kMxdTokens * kMxdMaxK];  // routing weights [t][s]
 };
 
-template <int PHASE>
+// One phase's stream-K geometry.
+struct PhaseGeo {
+    int R, K, MB, KG, rpi;          // rows per matrix, reduction, row blocks, K stages, rows per tile
+    long long U;                    // units
+    int G;                          // CTAs taking part (<= U, so every range holds a unit)
+    int u0, u1;                     // this CTA's range
+    int tile0, nseg;                // its first tile, its segments
+};
+
+__device__ __forceinline__ void phase_geo(PhaseGeo& g, int R, int K, int G2, int nt) {
+    g.R = R;
+    g.K = K;
+    g.rpi = G2 == 2 ? 128 : 256;
+    g.MB = mx_units(G2, R);
+    g.KG = mx_kg(K);
+    g.U = static_cast<long long>(nt) * g.MB * g.KG;
+    g.G = static_cast<int>(g.U < gridDim.x ? (g.U > 0 ? g.U : 1) : gridDim.x);
+    const bool in = static_cast<int>(blockIdx.x) < g.G;
+    g.u0 = in ? static_cast<int>(g.U * blockIdx.x / g.G) : 0;
+    g.u1 = in ? static_cast<int>(g.U * (blockIdx.x + 1) / g.G) : 0;
+    g.tile0 = g.u0 / g.KG;
+    g.nseg = g.u1 > g.u0 ? (g.u1 - 1) / g.KG - g.tile0 + 1 : 0;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int atom_acq_rel_gpu_add(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// touched experts the workspace was sized for
+__device__ __forceinline__ int nt_cap(const MxdArgs& a) { return a.E < a.T * a.k ? a.E : a.T * a.k; }
+
 __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant__ MxdParams P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const MxdArgs& a = P.a;
@@ -91,17 +144,10 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
     unsigned char* sfb = base + Ly.sfb_off;
     MxdTail* tl = reinterpret_cast<MxdTail*>(base + Ly.tail_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int G = PHASE == 0 ? 2 : 1;
-    constexpr int RPI = PHASE == 0 ? 128 : 256;       // weight rows per tile
-    const int R = a.R, K = a.K, T = a.T, k = a.k;
-    const int MB = mx_units(G, R);
-    const int KG = mx_kg(K);
+    const int T = a.T, k = a.k, E = a.E;
     const int NS = Ly.nslot;
-    const uint8_t* sfa_base = a.w + mx_sf_offset(G, a.E, R, K);
-    // Phase 1 reads idx and the x image; phase 2 reads idx early (the router finished before
-    // phase 1 passed its own wait, and phase 2 starts only after that) and waits before touching
-    // what phase 1 writes.
-    if (PHASE == 0) pdl_wait();
+    // idx, the routing weights, the x image and the counters come from earlier launches
+    pdl_wait();
     pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
@@ -116,6 +162,8 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
         }
         mbar_init(&tl->bready, 1);
         tl->abort_flag = 0;
+        tl->w0_issued = 0;
+        tl->w0_done = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -129,7 +177,7 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
         const int n = T * k;
         const int e0 = lane < n ? __ldcg(a.idx + lane) : -1;
         const int e1 = lane + 32 < n ? __ldcg(a.idx + lane + 32) : -1;
-        const bool v0 = e0 >= 0 && e0 < a.E, v1 = e1 >= 0 && e1 < a.E;
+        const bool v0 = e0 >= 0 && e0 < E, v1 = e1 >= 0 && e1 < E;
         if ((lane < n && !v0) || (lane + 32 < n && !v1)) report_error(a.status, DEV_ERR_INVALID);
         // touched experts as a bit mask (E <= 256), reduced over the warp; an expert's rank is
         // the number of touched experts below it
@@ -154,41 +202,40 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
         if (v0) { tl->touched[rank0] = e0; tl->rid[rank0][lane / k] = lane; }
         if (v1) { tl->touched[rank1] = e1; tl->rid[rank1][(lane + 32) / k] = lane + 32; }
         if (lane == 0) tl->nt = nt;
-        if (PHASE == 1) {
-            if (lane < n) tl->wr[lane] = __ldcg(a.wr + lane);
-            if (lane + 32 < n) tl->wr[lane + 32] = __ldcg(a.wr + lane + 32);
-        }
+        if (lane < n) tl->wr[lane] = __ldcg(a.wr + lane);
+        if (lane + 32 < n) tl->wr[lane + 32] = __ldcg(a.wr + lane + 32);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tl->tmem_base;
     const int nt = tl->nt;
-    const int tiles = nt * MB;
-    const long long U = static_cast<long long>(tiles) * KG;
-    // at most U CTAs take part, so that every range holds at least one unit (the part counts
-    // below assume it); the others have empty ranges
-    const int Gc = static_cast<int>(U < gridDim.x ? (U > 0 ? U : 1) : gridDim.x);
-    const bool in_grid = static_cast<int>(blockIdx.x) < Gc;
-    const int u0 = in_grid ? static_cast<int>(U * blockIdx.x / Gc) : 0;
-    const int u1 = in_grid ? static_cast<int>(U * (blockIdx.x + 1) / Gc) : 0;
-    // the CTA whose range holds unit u
-    auto cta_of = [&](long long u) { return static_cast<int>(((u + 1) * Gc + U - 1) / U - 1); };
+    // (two named structs, selected by value: an array indexed by the runtime phase would live in
+    // local memory)
+    PhaseGeo geo0, geo1;
+    phase_geo(geo0, a.I, a.H, 2, nt);
+    phase_geo(geo1, a.H, a.I, 1, nt);
+    const int nseg_all = geo0.nseg + geo1.nseg;
+    const int hdone = geo0.MB * 4;                // phase-1 slices of one expert's h
+    int* hcnt = a.cnt;
+    int* tcnt0 = a.cnt + nt_cap(a);
+    int* tcnt1 = tcnt0 + static_cast<size_t>(nt_cap(a)) * geo0.MB * 4;
+    int* rbcnt = tcnt1 + static_cast<size_t>(nt_cap(a)) * geo1.MB * 4;
 
-    // Segments: the maximal runs of one tile inside this CTA's range.  They are processed first,
-    // last, then the middle ones: the first and last segments are the ones that may share their
-    // tile with a neighbour, so their parts meet early and the CTA ends on a whole tile, whose
-    // finish needs no other CTA.
-    struct Seg { int tile, j, mb, kg0, kg1; };
-    const int tile0 = u0 / KG;
-    const int nseg_all = u1 > u0 ? (u1 - 1) / KG - tile0 + 1 : 0;
+    // Segments: the maximal runs of one tile inside a phase's range; segment i of the CTA's list
+    // is phase 1's (first, last, middle ones), then phase 2's.
+    struct Seg { int p, tile, j, mb, kg0, kg1; };
     auto seg_of = [&](int i, Seg& s) {
-        const int r = (i == 0 || nseg_all < 3) ? i : (i == 1 ? nseg_all - 1 : i - 1);
-        s.tile = tile0 + r;
-        s.kg0 = r == 0 ? u0 - tile0 * KG : 0;
-        s.kg1 = r == nseg_all - 1 ? u1 - s.tile * KG : KG;
-        s.j = s.tile / MB;
-        s.mb = s.tile - s.j * MB;
+        const int p = i < geo0.nseg ? 0 : 1;
+        const PhaseGeo g = p ? geo1 : geo0;
+        const int li = p ? i - geo0.nseg : i;
+        const int r = (li == 0 || g.nseg < 3) ? li : (li == 1 ? g.nseg - 1 : li - 1);
+        s.p = p;
+        s.tile = g.tile0 + r;
+        s.kg0 = r == 0 ? g.u0 - g.tile0 * g.KG : 0;
+        s.kg1 = r == g.nseg - 1 ? g.u1 - s.tile * g.KG : g.KG;
+        s.j = s.tile / g.MB;
+        s.mb = s.tile - s.j * g.MB;
     };
     // stage cursor over the segments
     struct Stage { int i, kg; Seg sg; };
@@ -200,52 +247,93 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
         c.kg = c.sg.kg0;
         return true;
     };
-    auto a_load = [&](int e, int mb, int kg, void* dst, uint64_t* bar) {
-        if (PHASE == 0) tma_load_5d(dst, &P.tmA, 0, mb * RPI, 0, kg, e, bar);
-        else tma_load_4d(dst, &P.tmA, 0, mb * RPI, kg, e, bar);
-    };
-    auto sfa_src = [&](int e, int mb, int kg) {
-        return sfa_base + ((static_cast<size_t>(e) * MB + mb) * KG + kg) * (2 * kDAtom);
+    auto sfa_src = [&](int p, int e, int mb, int kg) {
+        const PhaseGeo g = p ? geo1 : geo0;
+        const uint8_t* w = p ? a.wd : a.wgu;
+        return w + mx_sf_offset(p ? 1 : 2, E, g.R, g.K) +
+               ((static_cast<size_t>(e) * g.MB + mb) * g.KG + kg) * (2 * kDAtom);
     };
 
     if (warp == 0 || warp == 7) {
         if (lane == 0) {
-            // ================= producers: weight codes (warp 0), scale atoms (warp 7) ===========
+            // ================= producers: weight codes (warp 0), scales + B rows (warp 7) =======
+            // Both complete bytes on the slot's one barrier, whose expected count warp 0 sets
+            // for the whole stage (one barrier per slot measured faster than one per producer).
+            // A barrier only completes once both have issued, so warp 7 never leaves a stage
+            // that warp 0 issued without issuing its own copies for it: after an error it
+            // catches up with warp 0 (which stops at the error), then stops.
             const bool wts = warp == 0;
-            // warp 7 also copies each stage's B rows: the x image (phase 1; its scale atom once,
-            // first) or the split h stage with its atom (phase 2, after phase 1 has finished)
-            if (PHASE == 1 && !wts) pdl_wait();
-            if (PHASE == 0 && !wts) {
+            if (!wts) {
                 mbar_arrive_expect_tx(&tl->bready, kDAtom);
-                bulk_g2s(sfb, a.xs + static_cast<size_t>(KG) * kDBstage, kDAtom, &tl->bready);
+                bulk_g2s(sfb, a.xs + static_cast<size_t>(geo0.KG) * kDBstage, kDAtom, &tl->bready);
             }
             int it = 0;
             int issued[kDMaxSlots];
             for (int q = 0; q < kDMaxSlots; ++q) issued[q] = -1;
+            int jready = -1;                        // phase 2: the expert whose h is known complete
+            bool failed = false;                    // warp 7: an error stopped the stream
+            // warp 7 after an error: wait (bounded) until warp 0 has stopped; true while stage
+            // `it` is one warp 0 issued (so its barrier still needs warp 7's copies)
+            auto catch_up = [&]() {
+                const long long t0 = clock64();
+                while (!tl->w0_done && clock64() - t0 < (1ll << 31)) __nanosleep(256);
+                return it < tl->w0_issued;
+            };
             Stage c;
             first_stage(c);
             while (next_stage(c)) {
                 const int s = it % NS;
-                if (tl->abort_flag || !mbar_wait_bounded(&tl->empty[s], ((it / NS) & 1) ^ 1)) {
+                if (tl->abort_flag && !failed) {
+                    if (wts) break;
+                    failed = true;
+                }
+                if (failed && !catch_up()) break;
+                // (warp 7 cannot time out here on a stage warp 0 issued: warp 0 passed the same
+                // phase of this barrier, and it cannot advance further before the stage lands)
+                if (!mbar_wait_bounded(&tl->empty[s], ((it / NS) & 1) ^ 1)) {
                     tl->abort_flag = 1;
                     report_error(a.status, DEV_ERR_TIMEOUT);
                     break;
                 }
                 // test setting: the first stage's copies are withheld, so the consumers' bounded
                 // waits on it run out (reported as TS_ERR_TIMEOUT)
-                if (PHASE == 0 && a.stall && it == 0) {
+                if (a.stall && it == 0) {
                     ++it;
+                    if (wts) tl->w0_issued = it;
                     continue;
                 }
                 unsigned char* st = ring + static_cast<size_t>(s) * Ly.slot_bytes;
-                const int e = tl->touched[c.sg.j];
+                const Seg& sg = c.sg;
+                const int e = tl->touched[sg.j];
                 if (wts) {
-                    mbar_arrive_expect_tx(&tl->full[s], 2 * 8192 + 2 * kDAtom + (PHASE == 1 ? kMxdHImage : kDBstage));
-                    a_load(e, c.sg.mb, c.kg, st, &tl->full[s]);
+                    mbar_arrive_expect_tx(&tl->full[s], 2 * 8192 + 2 * kDAtom + (sg.p ? kMxdHImage : kDBstage));
+                    if (sg.p == 0) tma_load_5d(st, &P.tmA[0], 0, sg.mb * 128, 0, c.kg, e, &tl->full[s]);
+                    else tma_load_4d(st, &P.tmA[1], 0, sg.mb * 256, c.kg, e, &tl->full[s]);
+                    tl->w0_issued = it + 1;
                 } else {
-                    bulk_g2s(st + Ly.sfa_off, sfa_src(e, c.sg.mb, c.kg), 2 * kDAtom, &tl->full[s]);
-                    if (PHASE == 1)
-                        bulk_g2s(st + Ly.b_off, a.hs + (static_cast<size_t>(c.sg.j) * KG + c.kg) * kMxdHImage,
+                    if (sg.p == 1 && sg.j != jready && !failed) {
+                        // every phase-1 slice of this expert's h has been written
+                        const long long t0 = clock64();
+                        bool ok = true;
+                        while (ld_acquire_gpu(hcnt + sg.j) < hdone) {
+                            if (tl->abort_flag || clock64() - t0 > (1ll << 31)) { ok = false; break; }
+                            __nanosleep(128);
+                        }
+                        if (ok) {
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            jready = sg.j;
+                        } else {
+                            tl->abort_flag = 1;
+                            report_error(a.status, DEV_ERR_TIMEOUT);
+                            failed = true;
+                            // the copies below still go out (with whatever the h image holds:
+                            // the call's outputs are void) if warp 0 issued this stage
+                            if (!catch_up()) break;
+                        }
+                    }
+                    bulk_g2s(st + Ly.sfa_off, sfa_src(sg.p, e, sg.mb, c.kg), 2 * kDAtom, &tl->full[s]);
+                    if (sg.p == 1)
+                        bulk_g2s(st + Ly.b_off, a.hs + (static_cast<size_t>(sg.j) * geo1.KG + c.kg) * kMxdHImage,
                                  kMxdHImage, &tl->full[s]);
                     else
                         bulk_g2s(st + Ly.b_off, a.xs + static_cast<size_t>(c.kg) * kDBstage, kDBstage, &tl->full[s]);
@@ -253,37 +341,31 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                 issued[s] = it;
                 ++it;
             }
-            for (int q = 0; q < NS; ++q)
-                if (issued[q] >= 0) mbar_wait_bounded(&tl->full[q], (issued[q] / NS) & 1);
+            if (wts) {
+                tl->w0_done = 1;
+                // no copy may be in flight when the CTA exits: every stage warp 0 issued is also
+                // issued by warp 7 (above), so each barrier completes
+                for (int q = 0; q < NS; ++q)
+                    if (issued[q] >= 0) mbar_wait_bounded(&tl->full[q], (issued[q] / NS) & 1);
+            } else {
+                mbar_wait_bounded(&tl->bready, 0);
+            }
         }
     } else if (warp == 6) {
         // ===================== scale atoms into TMEM, one commit per stage =====================
-        int it = 0;
-        bool stop = false;
-        if (PHASE == 0) {
-            // the resident x scales, once
-            int ok = 1;
-            if (lane == 0) {
-                ok = mbar_wait_bounded(&tl->bready, 0);
-                if (ok) {
-                    tc_fence_after();
-                    tmem_cp_atom(tmem + kDColSfb, sfb);
-                }
+        if (lane == 0) {
+            bool stop = !mbar_wait_bounded(&tl->bready, 0);
+            if (!stop) {
+                tc_fence_after();
+                tmem_cp_atom(tmem + kDColSfb, sfb);     // the x scales, once
             }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                if (lane == 0) { tl->abort_flag = 1; report_error(a.status, DEV_ERR_TIMEOUT); }
-                stop = true;
-            }
-        }
-        if (lane == 0 && !stop) {
+            int it = 0;
             for (int i = 0; i < nseg_all && !stop; ++i) {
                 Seg sg;
                 seg_of(i, sg);
                 for (int kg = sg.kg0; kg < sg.kg1; ++kg, ++it) {
                     const int s = it % NS;
                     if (tl->abort_flag || !mbar_wait_bounded(&tl->full[s], (it / NS) & 1)) {
-                        tl->abort_flag = 1;
-                        report_error(a.status, DEV_ERR_TIMEOUT);
                         stop = true;
                         break;
                     }
@@ -292,28 +374,29 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                     const uint32_t tsf = tmem + kDColSf + 16u * s;
                     tmem_cp_atom(tsf, st + Ly.sfa_off);
                     tmem_cp_atom(tsf + 4, st + Ly.sfa_off + kDAtom);
-                    if (PHASE == 1) tmem_cp_atom(tsf + 8, st + Ly.b_off + kDBstage);
+                    if (sg.p == 1) tmem_cp_atom(tsf + 8, st + Ly.b_off + kDBstage);
                     umma_commit(&tl->sfull[s]);
                 }
+            }
+            if (stop) {
+                tl->abort_flag = 1;
+                report_error(a.status, DEV_ERR_TIMEOUT);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ================================= MMA issuer ====================================
-            bool ok = PHASE == 1 || mbar_wait_bounded(&tl->bready, 0);
-            if (!ok) { tl->abort_flag = 1; report_error(a.status, DEV_ERR_TIMEOUT); }
+            bool ok = true;
             int it = 0;
             for (int nseg = 0; nseg < nseg_all && ok && !tl->abort_flag; ++nseg) {
                 Seg sg;
                 seg_of(nseg, sg);
-                const bool has1 = PHASE == 0 || sg.mb * RPI + 128 < R;
+                const bool has1 = sg.p == 0 || sg.mb * 256 + 128 < a.H;
                 const int tb = nseg & 1;
                 const uint32_t acc0 = tmem + static_cast<uint32_t>(tb * 32);
                 const uint32_t acc1 = acc0 + 16;
-
                 if (!mbar_wait_bounded(&tl->tempty[tb], ((nseg >> 1) & 1) ^ 1)) {
-                    tl->abort_flag = 1;
-                    report_error(a.status, DEV_ERR_TIMEOUT);
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
@@ -321,15 +404,13 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                     const int s = it % NS;
                     if (!mbar_wait_bounded(&tl->full[s], (it / NS) & 1) ||
                         !mbar_wait_bounded(&tl->sfull[s], (it / NS) & 1)) {
-                        tl->abort_flag = 1;
-                        report_error(a.status, DEV_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const unsigned char* st = ring + static_cast<size_t>(s) * Ly.slot_bytes;
                     const uint32_t tsf = tmem + kDColSf + 16u * s;
-                    const uint32_t tsfb = PHASE == 0 ? tmem + kDColSfb : tsf + 8;
+                    const uint32_t tsfb = sg.p == 0 ? tmem + kDColSfb : tsf + 8;
                     const uint64_t dA0 = sdesc_sw128(smem_u32(st));
                     const uint64_t dA1 = sdesc_sw128(smem_u32(st + kDAbox));
                     const uint64_t dB = sdesc_sw128(smem_u32(st + Ly.b_off));
@@ -345,15 +426,19 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                 if (!ok) break;
                 umma_commit(&tl->tfull[tb]);
             }
+            if (!ok) {
+                tl->abort_flag = 1;
+                report_error(a.status, DEV_ERR_TIMEOUT);
+            }
         }
     } else {
         // =================================== epilogue ==========================================
         const int q = warp & 3;                     // TMEM lane quarter: rows 32q .. 32q + 31
-        if (PHASE == 1) pdl_wait();                // parts, counters and e of phase 1's launch
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
         for (int nseg = 0; nseg < nseg_all; ++nseg) {
             Seg sg;
             seg_of(nseg, sg);
+            const PhaseGeo g = sg.p ? geo1 : geo0;
             const int tb = nseg & 1;
             const bool go = __shfl_sync(0xffffffffu, tl->abort_flag, 0) == 0;
             if (!__all_sync(0xffffffffu, go && mbar_wait_bounded(&tl->tfull[tb], (nseg >> 1) & 1))) {
@@ -374,11 +459,11 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                 x1[t] = d1[t] + d1b[t];
             }
             const int e = tl->touched[sg.j];
-            const int ra = sg.mb * RPI + 32 * q + lane;      // row of acc0 (acc1: + 128, phase 2)
-            if (!(sg.kg0 == 0 && sg.kg1 == KG)) {
+            const int ra = sg.mb * g.rpi + 32 * q + lane;    // row of acc0 (acc1: + 128, phase 2)
+            if (!(sg.kg0 == 0 && sg.kg1 == g.KG)) {
                 // a tile split between CTAs: park this part; the last part's CTA finishes
-                const int slot = (u0 >= sg.tile * KG) ? 0 : 1;   // this CTA's first or last segment
-                float* pp = a.part + ((static_cast<size_t>(blockIdx.x) * 2 + slot) * 2) * 128 * 8;
+                const int slot = (g.u0 >= sg.tile * g.KG) ? 0 : 1;   // this CTA's first or last segment
+                float* pp = a.part + ((static_cast<size_t>(blockIdx.x) * 2 + sg.p) * 2 + slot) * kMxdPartFloats;
                 float4* p0 = reinterpret_cast<float4*>(pp + (32 * q + lane) * 8);
                 float4* p1 = reinterpret_cast<float4*>(pp + (128 + 32 * q + lane) * 8);
                 p0[0] = make_float4(x0[0], x0[1], x0[2], x0[3]);
@@ -387,15 +472,15 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                 p1[1] = make_float4(x1[4], x1[5], x1[6], x1[7]);
                 // the warp barrier orders the lanes' stores before lane 0's release
                 __syncwarp();
-                const long long tu0 = static_cast<long long>(sg.tile) * KG;
-                const int b0 = cta_of(tu0), b1 = cta_of(tu0 + KG - 1);
+                const long long tu0 = static_cast<long long>(sg.tile) * g.KG;
+                // the CTAs b0 .. b1 whose ranges hold the tile's units
+                const int b0 = static_cast<int>(((tu0 + 1) * g.G + g.U - 1) / g.U - 1);
+                const int b1 = static_cast<int>(((tu0 + g.KG) * g.G + g.U - 1) / g.U - 1);
                 int last = 0;
                 if (lane == 0) {
-                    int old;
-                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old)
-                                 : "l"(a.tcnt + sg.tile * 4 + q) : "memory");
-                    last = old + 1 == b1 - b0 + 1;
-                    if (last) a.tcnt[sg.tile * 4 + q] = 0;
+                    int* cp = (sg.p ? tcnt1 : tcnt0) + sg.tile * 4 + q;
+                    last = atom_acq_rel_gpu_add(cp, 1) + 1 == b1 - b0 + 1;
+                    if (last) *cp = 0;
                 }
                 if (!__shfl_sync(0xffffffffu, last, 0)) continue;
                 __syncwarp();                       // lane 0's acquire, then every lane's loads
@@ -412,8 +497,8 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                             for (int i = 0; i < 4; ++i) pv[bb][i] = make_float4(0.f, 0.f, 0.f, 0.f);
                             continue;
                         }
-                        const int bslot = (static_cast<long long>(U * (b + bb) / Gc) >= tu0) ? 0 : 1;
-                        const float* qp = a.part + ((static_cast<size_t>(b + bb) * 2 + bslot) * 2) * 128 * 8;
+                        const int bslot = (static_cast<long long>(g.U * (b + bb) / g.G) >= tu0) ? 0 : 1;
+                        const float* qp = a.part + ((static_cast<size_t>(b + bb) * 2 + sg.p) * 2 + bslot) * kMxdPartFloats;
                         const float4* q0 = reinterpret_cast<const float4*>(qp + (32 * q + lane) * 8);
                         const float4* q1 = reinterpret_cast<const float4*>(qp + (128 + 32 * q + lane) * 8);
                         pv[bb][0] = __ldcg(q0);
@@ -431,20 +516,21 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                     }
                 }
             }
-            if (PHASE == 0) {
-                // ---- finish: bias, activation, h rounded to bf16, then split for phase 2: this
-                // 128-row tile is K stage mb of phase 2 (B rows plane * 8 + t, 128-byte swizzle),
-                // warp q's 32 rows its scale block q ----
-                unsigned char* img = a.hs + (static_cast<size_t>(sg.j) * MB + sg.mb) * kMxdHImage;
-                const bool live = sg.mb * RPI + 32 * q < R;          // rows past I stay zero
+            if (sg.p == 0) {
+                // ---- phase 1 finish: bias, activation, h rounded to bf16, then split for phase 2:
+                // this 128-row tile is K stage mb of phase 2 (B rows plane * 8 + t, 128-byte
+                // swizzle), warp q's 32 rows its scale block q ----
+                const int R = a.I;
+                unsigned char* img = a.hs + (static_cast<size_t>(sg.j) * g.MB + sg.mb) * kMxdHImage;
+                const bool live = sg.mb * 128 + 32 * q < R;          // rows past I stay zero
                 float hv[8];
                 if (live) {
                     const size_t bi = static_cast<size_t>(e) * R + ra;
-                    const float bg = a.b0 ? __bfloat162float(__ushort_as_bfloat16(a.b0[bi])) : 0.0f;
-                    const float bu = a.b1 ? __bfloat162float(__ushort_as_bfloat16(a.b1[bi])) : 0.0f;
+                    const float bgv = a.bg ? __bfloat162float(__ushort_as_bfloat16(a.bg[bi])) : 0.0f;
+                    const float buv = a.bu ? __bfloat162float(__ushort_as_bfloat16(a.bu[bi])) : 0.0f;
 #pragma unroll
                     for (int t = 0; t < 8; ++t)
-                        hv[t] = __bfloat162float(__float2bfloat16_rn(act_fn(a.act, x0[t] + bg, x1[t] + bu, a.limit, a.alpha)));
+                        hv[t] = __bfloat162float(__float2bfloat16_rn(act_fn(a.act, x0[t] + bgv, x1[t] + buv, a.limit, a.alpha)));
                 } else {
 #pragma unroll
                     for (int t = 0; t < 8; ++t) hv[t] = 0.0f;
@@ -473,12 +559,19 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                     img[kDBstage + 16 * lane + q] = static_cast<unsigned char>(se_mine + 127);
                     img[kDBstage + 16 * (8 + lane) + q] = static_cast<unsigned char>(se_mine + 123);
                 }
+                // phase 2 copies the image with the async proxy: order these stores before the
+                // release that publishes the slice
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) red_release_gpu_add(hcnt + sg.j, 1);
             } else {
-                // ---- finish: bias, e per route; the last tile of a row block runs its combine ----
+                // ---- phase 2 finish: bias, e per route; the last tile of a row block runs its
+                // combine ----
+                const int R = a.H;
                 const int rb = ra + 128;
-                const bool va = sg.mb * RPI + 32 * q < R, vb = sg.mb * RPI + 128 + 32 * q < R;
-                const float bga = (a.b0 && va) ? __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + ra])) : 0.0f;
-                const float bgb = (a.b0 && vb) ? __bfloat162float(__ushort_as_bfloat16(a.b0[static_cast<size_t>(e) * R + rb])) : 0.0f;
+                const bool va = sg.mb * 256 + 32 * q < R, vb = sg.mb * 256 + 128 + 32 * q < R;
+                const float bga = (a.bd && va) ? __bfloat162float(__ushort_as_bfloat16(a.bd[static_cast<size_t>(e) * R + ra])) : 0.0f;
+                const float bgb = (a.bd && vb) ? __bfloat162float(__ushort_as_bfloat16(a.bd[static_cast<size_t>(e) * R + rb])) : 0.0f;
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int r = tl->rid[sg.j][t];
@@ -489,57 +582,66 @@ __global__ void __launch_bounds__(kDThreads, 1) mxd_kernel(const __grid_constant
                 __syncwarp();                       // the lanes' stores, then lane 0's release
                 int last = 0;
                 if (lane == 0) {
-                    int old;
-                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old)
-                                 : "l"(a.rbcnt + sg.mb * 4 + q) : "memory");
-                    last = old + 1 == nt;
-                    if (last) a.rbcnt[sg.mb * 4 + q] = 0;
+                    int* cp = rbcnt + sg.mb * 4 + q;
+                    last = atom_acq_rel_gpu_add(cp, 1) + 1 == nt;
+                    if (last) *cp = 0;
                 }
                 if (__shfl_sync(0xffffffffu, last, 0)) {
                     __syncwarp();                   // lane 0's acquire, then every lane's loads
-                    // slot-ordered combine of this slice's rows (ra, rb) for every token: the
-                    // loads of four slots of all tokens are issued before their sums
+                    // slot-ordered combine of this slice's 64 rows (32 at ra, 32 at rb) for every
+                    // token: item i = (token, 4-row group) with float4 loads of e, 4 items per
+                    // lane, all of a slot group's loads issued before their sums
                     uint16_t* y = static_cast<uint16_t*>(a.y);
-                    float acc[kMxdTokens][2];
+                    const int base0 = sg.mb * 256 + 32 * q;
+                    float4 acc[4];
+                    int yo[4];
+                    bool vi[4];
 #pragma unroll
-                    for (int t = 0; t < kMxdTokens; ++t)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const bool v = t < T && (hh ? vb : va);
-                            acc[t][hh] = (v && a.seed) ? __ldcg(a.seed + static_cast<size_t>(t) * R + (hh ? rb : ra)) : 0.0f;
-                        }
+                    for (int m = 0; m < 4; ++m) {
+                        const int i = lane + 32 * m;               // 0..127
+                        const int t = i >> 4, g = i & 15;
+                        const int row = base0 + (g >> 3) * 128 + 4 * (g & 7);
+                        vi[m] = t < T && ((g >> 3) ? vb : va);
+                        yo[m] = t * R + row;
+                        acc[m] = (vi[m] && a.seed) ? __ldcg(reinterpret_cast<const float4*>(a.seed + yo[m]))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                     for (int s0 = 0; s0 < k; s0 += 4) {
-                        float ev[kMxdTokens][2][4];
+                        float4 ev[4][4];
 #pragma unroll
-                        for (int t = 0; t < kMxdTokens; ++t)
+                        for (int m = 0; m < 4; ++m)
 #pragma unroll
                             for (int s = 0; s < 4; ++s) {
-                                const bool vt = t < T && s0 + s < k;
-                                const float* src = a.e_out + static_cast<size_t>(vt ? t * k + s0 + s : 0) * R;
-                                ev[t][0][s] = (vt && va) ? __ldcg(src + ra) : 0.0f;
-                                ev[t][1][s] = (vt && vb) ? __ldcg(src + rb) : 0.0f;
+                                const int t = (lane + 32 * m) >> 4;
+                                const bool v = vi[m] && s0 + s < k;
+                                const float* src = a.e_out + static_cast<size_t>(v ? t * k + s0 + s : 0) * R +
+                                                   (yo[m] - t * R);
+                                ev[m][s] = v ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
 #pragma unroll
-                        for (int t = 0; t < kMxdTokens; ++t)
+                        for (int m = 0; m < 4; ++m)
 #pragma unroll
                             for (int s = 0; s < 4; ++s) {
-                                const bool vt = t < T && s0 + s < k;
-                                const float wv = tl->wr[vt ? t * k + s0 + s : 0];
-                                const float n0 = __fadd_rn(acc[t][0], __fmul_rn(wv, ev[t][0][s]));
-                                const float n1 = __fadd_rn(acc[t][1], __fmul_rn(wv, ev[t][1][s]));
-                                acc[t][0] = vt ? n0 : acc[t][0];
-                                acc[t][1] = vt ? n1 : acc[t][1];
+                                const int t = (lane + 32 * m) >> 4;
+                                if (!vi[m] || s0 + s >= k) continue;
+                                const float wv = tl->wr[t * k + s0 + s];
+                                acc[m].x = __fadd_rn(acc[m].x, __fmul_rn(wv, ev[m][s].x));
+                                acc[m].y = __fadd_rn(acc[m].y, __fmul_rn(wv, ev[m][s].y));
+                                acc[m].z = __fadd_rn(acc[m].z, __fmul_rn(wv, ev[m][s].z));
+                                acc[m].w = __fadd_rn(acc[m].w, __fmul_rn(wv, ev[m][s].w));
                             }
                     }
 #pragma unroll
-                    for (int t = 0; t < kMxdTokens; ++t)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            if (t >= T || !(hh ? vb : va)) continue;
-                            const size_t yo = static_cast<size_t>(t) * R + (hh ? rb : ra);
-                            if (a.y_f32) a.y_f32[yo] = acc[t][hh];
-                            y[yo] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[t][hh]));
-                        }
+                    for (int m = 0; m < 4; ++m) {
+                        if (!vi[m]) continue;
+                        if (a.y_f32) *reinterpret_cast<float4*>(a.y_f32 + yo[m]) = acc[m];
+                        const uint2 o = make_uint2(
+                            static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[m].x))) |
+                                (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[m].y))) << 16),
+                            static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[m].z))) |
+                                (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[m].w))) << 16));
+                        *reinterpret_cast<uint2*>(y + yo[m]) = o;
+                    }
                 }
             }
         }
@@ -579,9 +681,9 @@ inline bool make_map_mxd_codes(CUtensorMap* m, const void* blob, int G, int K, i
 __global__ void __launch_bounds__(256) mxd_prep_kernel(const MxdArgs a) {
     pdl_wait();
     pdl_launch_dependents();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.ncnt; i += gridDim.x * blockDim.x) a.tcnt[i] = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.ncnt; i += gridDim.x * blockDim.x) a.cnt[i] = 0;
     __shared__ float red[8];
-    const int t = blockIdx.x, c = threadIdx.x, K = a.K, KG = mx_kg(K);
+    const int t = blockIdx.x, c = threadIdx.x, K = a.H, KG = mx_kg(K);
     uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
     if (t < a.T && c * 16 < K) {
         const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * K + c * 16);
@@ -630,7 +732,7 @@ __global__ void __launch_bounds__(256) mxd_prep_kernel(const MxdArgs a) {
 }  // namespace
 
 cudaError_t launch_mxd_prep(const MxdArgs& a, cudaStream_t s) {
-    if (a.K > kMxdMaxH || a.T > kMxdTokens) return cudaErrorInvalidValue;
+    if (a.H > kMxdMaxH || a.T > kMxdTokens) return cudaErrorInvalidValue;
     return launch_pdl(mxd_prep_kernel, dim3(kMxdTokens), dim3(256), 0, s, a);
 }
 
@@ -639,31 +741,42 @@ cudaError_t launch_mxd(const MxdArgs& a, int num_sms, cudaStream_t s) {
     memset(&P, 0, sizeof(P));
     P.a = a;
     MxdLayout& L = P.ly;
-    const int KG = mx_kg(a.K);
     L.sfa_off = 2 * kDAbox;
     L.b_off = L.sfa_off + 2 * kDAtom;
-    L.slot_bytes = (L.b_off + (a.phase == 1 ? kMxdHImage : kDBstage) + 1023) / 1024 * 1024;
+    L.slot_bytes = (L.b_off + kMxdHImage + 1023) / 1024 * 1024;
     const size_t tail = (sizeof(MxdTail) + 255) / 256 * 256;
     const size_t fixed = kDAtom + tail;
     const size_t budget = 227 * 1024 - 1024;
-    if (fixed >= budget) return cudaErrorInvalidValue;
     L.nslot = static_cast<int>((budget - fixed) / L.slot_bytes);
     if (L.nslot > kDMaxSlots) L.nslot = kDMaxSlots;
     if (L.nslot < 2) return cudaErrorInvalidValue;
     L.sfb_off = L.nslot * L.slot_bytes;
     L.tail_off = L.sfb_off + kDAtom;
     const size_t smem = 1024 + static_cast<size_t>(L.tail_off) + tail;
-    if (!make_map_mxd_codes(&P.tmA, a.w, a.phase == 0 ? 2 : 1, a.K, a.R, a.E)) return cudaErrorInvalidValue;
-    const int grid = num_sms < kMxdMaxCtas ? num_sms : kMxdMaxCtas;
-    cudaError_t e;
-    if (a.phase == 0) {
-        e = ensure_smem(mxd_kernel<0>, smem);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(mxd_kernel<0>, dim3(grid), dim3(kDThreads), smem, s, P);
-    }
-    e = ensure_smem(mxd_kernel<1>, smem);
+    if (!make_map_mxd_codes(&P.tmA[0], a.wgu, 2, a.H, a.I, a.E)) return cudaErrorInvalidValue;
+    if (!make_map_mxd_codes(&P.tmA[1], a.wd, 1, a.I, a.H, a.E)) return cudaErrorInvalidValue;
+    cudaError_t e = ensure_smem(mxd_kernel, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(mxd_kernel<1>, dim3(grid), dim3(kDThreads), smem, s, P);
+    // one CTA per SM, all resident (cooperative): phase 2's producers wait for phase-1 tiles of
+    // other CTAs
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxd_kernel, kDThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidValue;
+    const int grid = num_sms < kMxdMaxCtas ? num_sms : kMxdMaxCtas;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, mxd_kernel, P);
 }
 
 }  // namespace tsmoe

@@ -195,38 +195,41 @@ cudaError_t launch_mx_split_rows(const uint16_t* x, const int32_t* perm, int k, 
 cudaError_t launch_mx_pack(int G, int nmat, int R, int K, const uint8_t* codes0, const uint8_t* scales0,
                            const uint8_t* codes1, const uint8_t* scales1, uint8_t* blob, cudaStream_t s);
 
-// Decode batches (T <= 8) with MXFP4 experts and bf16 activations (gemm_mxd.cu): two launches
-// over the touched experts, every touched expert's weights streamed once.
+// Decode batches (T <= 8) with MXFP4 experts and bf16 activations (gemm_mxd.cu): a prep launch
+// (x split, counters zeroed), then one persistent cooperative launch running both phases over
+// the touched experts, every touched expert's weights streamed once.
 constexpr int kMxdTokens = 8;        // token rows per term plane
 constexpr int kMxdMaxTouched = 64;   // touched experts <= min(E, T*k) <= 64
 constexpr int kMxdMaxCtas = 256;     // stream-K partial slots
 constexpr int kMxdMaxK = 8;          // routes per token
-constexpr int kMxdMaxH = 4096;       // phase 1 keeps the split token rows resident (K <= 4096)
+constexpr int kMxdAutoMinT = 3;      // TS_PATH_AUTO takes the decode kernels from this many tokens
+constexpr int kMxdMaxH = 4096;       // the prep kernel takes a token row per 256 threads x 16
 constexpr int kMxdBStage = 2 * kMxdTokens * 128;        // one K stage of B: 16 rows x 128 bytes
 constexpr int kMxdHImage = kMxdBStage + 512;            // + its scale atom
+constexpr size_t kMxdPartFloats = 2 * 128 * 8;          // one parked part: 2 x 128 rows x 8 tokens
 struct MxdArgs {
-    int phase;                    // 0: gate/up + act -> h; 1: down -> e, slot-ordered combine
     int act;
     float limit, alpha;
-    const uint8_t* w;             // tensor-core blob: phase 0 gate + up (G = 2), phase 1 down (G = 1)
-    const uint16_t* b0;           // phase 0 gate bias / phase 1 down bias ([E][R] bf16) or nullptr
-    const uint16_t* b1;           // phase 0 up bias or nullptr
-    int R, K, E, T, k;            // rows per matrix, reduction length, experts, tokens, routes/token
+    const uint8_t* wgu;           // tensor-core blob of gate + up (G = 2)
+    const uint8_t* wd;            // tensor-core blob of down (G = 1)
+    const uint16_t* bg;           // biases [E][I], [E][I], [E][H] bf16, or nullptr
+    const uint16_t* bu;
+    const uint16_t* bd;
+    int H, I, E, T, k;            // hidden, intermediate, experts, tokens, routes per token
     const int32_t* idx;           // [T][k]
     const float* wr;              // routing weights [T][k]
-    const uint16_t* x;            // prep: [T][K] bf16
-    uint8_t* xs;                  // x image: [ceil(K/128)][16][128 B] + a 512 B scale atom
+    const uint16_t* x;            // prep: [T][H] bf16
+    uint8_t* xs;                  // x image: [ceil(H/128)][16][128 B] + a 512 B scale atom
     uint8_t* hs;                  // h images: [min(E, T*k)][ceil(I/128)][kMxdHImage]
-    float* e_out;                 // phase 1: e [T*k][H] f32 by route id
+    float* e_out;                 // e [T*k][H] f32 by route id
     const float* seed;            // combine seed [T][H] f32 or nullptr
     void* y;                      // [T][H] bf16
     float* y_f32;                 // [T][H] or nullptr
-    float* part;                  // stream-K partials [kMxdMaxCtas][2][2][128][8] f32
-    int* tcnt;                    // per (tile, 32-row slice) part counters, zero between calls
-    int ncnt;                     // prep: counters to zero from tcnt on (part + row-block)
-    int* rbcnt;                   // phase 1: per (row block, slice) finished-tile counters
+    float* part;                  // stream-K partials [kMxdMaxCtas][2 phases][2][kMxdPartFloats]
+    int* cnt;                     // counters, zero on entry (the prep kernel zeroes ncnt of them):
+    int ncnt;                     //   [hcnt: nt][tcnt0: nt*MB0*4][tcnt1: nt*MB1*4][rbcnt: MB1*4]
     int* status;
-    int stall;                    // test setting: phase 1 withholds its first stage's copies
+    int stall;                    // test setting: the first stage's copies are withheld
 };
 cudaError_t launch_mxd(const MxdArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_mxd_prep(const MxdArgs& a, cudaStream_t s);

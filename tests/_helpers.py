@@ -146,9 +146,10 @@ def kappa_for(cfg, T, path):
     tc_fmt = cfg["fmt"] == "mxfp4" or cfg["fmt"] == cfg["adt"]
     tc_shape = cfg["H"] % 64 == 0 and cfg["I"] % 64 == 0
     mx = cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
-    # block-scaled decode kernels: "gemm" or "auto" at T <= 8 (MXFP4 + bf16, T*k <= 64, k <= 8,
-    # H <= 4096)
-    mxd = mx and T <= 8 and T * cfg["k"] <= 64 and cfg["k"] <= 8 and cfg["H"] <= 4096 and path in ("gemm", "auto")
+    # block-scaled decode kernels: "gemm" at T <= 8, "auto" at 3 <= T <= 8 (MXFP4 + bf16,
+    # T*k <= 64, k <= 8, H <= 4096)
+    mxd = (mx and T <= 8 and T * cfg["k"] <= 64 and cfg["k"] <= 8 and cfg["H"] <= 4096
+           and (path == "gemm" or (path == "auto" and T >= 3)))
     tc = mxd or ((path in ("gemm", "gemm_dequant") or (path == "auto" and T > 8)) and (mx or (tc_fmt and tc_shape)))
     return KAPPA_TC if tc else KAPPA_GEMV
 # f32 evaluation of the activation itself (expf / tanhf, a divide, two multiplies), relative
