@@ -322,13 +322,13 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     torch.cuda.synchronize()
 
     def step(ly, stream=None):
+        # the whole layer through ts_moe_route_forward: the router, then the experts (the router's
+        # step runs inside the decode kernels' prep launch when they take the call)
         L = ly["L"]
-        moe.router_route(L["x"], L["Wr"], k, mode=cfg["mode"], router_bias=L["router_bias"],
-                         per_expert_scale=L["scale"], rmsnorm=cfg["rmsnorm"],
-                         out=(ly["idx"], ly["w"], ly["xn"], None), stream=stream)
-        xin = ly["xn"] if cfg["rmsnorm"] else L["x"]
-        moe.forward(xin, ly["ex"], ly["idx"], ly["w"], shared=ly["sh"], ws=ly["ws"],
-                    out=(ly["y"], None), path=args.path, stream=stream)
+        moe.route_forward(L["x"], L["Wr"], k, ly["ex"], mode=cfg["mode"], router_bias=L["router_bias"],
+                          per_expert_scale=L["scale"], rmsnorm=cfg["rmsnorm"], shared=ly["sh"],
+                          ws=ly["ws"], path=args.path,
+                          out=(ly["y"], None, ly["idx"], ly["w"], ly["xn"]), stream=stream)
         if args.gemma_tail:
             moe.gemma_tail(ly["y"], ly["h1"], ly["xres"], ly["w_post2"], ly["w_post"], 0.5,
                            stream=stream)
@@ -374,7 +374,9 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # "gemm_dequant" the f16 MMA over dequantised weights (gather, h conversion)
     mx_path = (gemm_path and not mxd_path and cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
                and args.path != "gemm_dequant")
-    n_launch_step = ((3 if mxd_path else 3 if fused_decode else 5 + (1 if gemm_path else 0)
+    # the decode kernels' prep (x split, counters) done by the router launch
+    route_fold = mxd_path
+    n_launch_step = ((2 if route_fold else 3 if mxd_path else 3 if fused_decode else 5 + (1 if gemm_path else 0)
                       + (1 if gemm_path and cfg["fmt"] == "mxfp4" and not mx_path else 0))
                      + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail else 0))
 
@@ -416,8 +418,8 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # ---- per-phase breakdown: graphs carrying event-record nodes after every launch ----------------
     # event order in a step: 6 router, 0 route list, 1 phase 1, [2 shared phase 1], 3 phase 2,
     # [4 shared phase 2], 5 combine, [7 Gemma sandwich tail]
-    if mxd_path:   # router, prep, [shared phase 1, shared phase 2], both phases + combine
-        order = [6, 0] + ([2, 4] if cfg.get("shared_I") else []) + [1]
+    if mxd_path:   # router (+ prep), [shared phase 1, shared phase 2], both phases + combine
+        order = [6] + ([] if route_fold else [0]) + ([2, 4] if cfg.get("shared_I") else []) + [1]
     elif gemm_path:
         order = [6, 0, 1, 3, 5]
     else:   # GEMV: routed phase 1, shared phase 1, shared phase 2, routed phase 2 (+ combine)
@@ -436,9 +438,9 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
             samples[moe.PHASES[j]].append(prev.elapsed_time(phase_ev[j]))
             prev = phase_ev[j]
     phases = {n: statistics.mean(v) for n, v in samples.items()}
-    if mxd_path:   # the prep launch splits x (no route list); one launch runs both phases
-        phases = {("prep_x_split" if n == "route_list" else "experts_fused" if n == "experts_phase1"
-                   else n): v for n, v in phases.items()}
+    if mxd_path:   # the router launch splits x as well; one launch runs both phases
+        phases = {("router_and_prep" if n == "router" and route_fold else "prep_x_split" if n == "route_list"
+                   else "experts_fused" if n == "experts_phase1" else n): v for n, v in phases.items()}
 
     # ---- algorithmic bytes / FLOPs of the dominant kernel (expert phase 1) ---------------------------
     idx_np = layers[0]["idx"].cpu().numpy()
@@ -524,7 +526,8 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
                      "frac": step_bytes / (ms_max * 1e-3) / 1e9 / hbm_peak},
         "dtype": dtype_label(cfg, gemm_path, mx_path or mxd_path), "workload": wl, "cfg": cfg,
         "path": ("tcgen05 block-scaled decode kernels (kind::mxf8f6f4, stream-K over every SM, TMA + TMEM; "
-                 "prep, gate/up, down + fused combine)" if mxd_path
+                 + ("router launch with the prep folded in, " if route_fold else "prep, ")
+                 + "gate/up, down + fused combine)" if mxd_path
                  else "tcgen05 block-scaled grouped GEMM (kind::mxf8f6f4, TMA + TMEM)" if mx_path
                  else "tcgen05 grouped GEMM (TMA + TMEM)" if gemm_path
                  else "gemv (mma.sync m16n8k16 over streamed tiles)"),

@@ -256,6 +256,21 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
                               const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
                               size_t ws_bytes, int32_t path, void* stream);
 
+/* The whole routed layer from x: ts_moe_router_route, then ts_moe_forward_path on its idx / w
+ * (and on xn when rmsnorm is 1), with the same arguments, meaning and results: idx and w are
+ * written as ts_moe_router_route writes them, y as ts_moe_forward writes it.  When the
+ * block-scaled decode kernels take the call (MXFP4 experts, bf16, T <= 8; see TS_PATH_AUTO /
+ * TS_PATH_GEMM), the router launch also does their prep (the x rows, after the RMSNorm when
+ * on, split into the kernels' e4m3 image; their counters zeroed), so the layer without a
+ * shared expert is two launches; otherwise the router launch is followed by the forward's.
+ * H and E come from the experts; x is H columns wide.  T == 0 launches nothing.          */
+ts_status ts_moe_route_forward(const void* x, int32_t adt, int32_t T, const void* W_r,
+                               int32_t rmsnorm, float eps, const float* router_bias,
+                               const float* per_expert_scale, int32_t k, int32_t mode,
+                               const ts_moe_experts* ex, const ts_moe_experts* shared,
+                               void* xn_out, int32_t* idx, float* w, void* y, float* y_f32,
+                               void* ws, size_t ws_bytes, int32_t path, void* stream);
+
 /* As ts_moe_forward (automatic path), for callers that cannot allocate device memory: instead
  * of a caller-provided workspace it uses a scratch array that lives in the library's own device
  * memory (16 MiB per GPU, held until the process exits).  The source pages have no counterpart;

@@ -74,6 +74,8 @@ def lib():
                                ctypes.c_int),
             "ts_moe_forward_path": ([vp, i32, i32, pe, vp, vp, i32, pe, vp, vp, vp, sz, i32, vp],
                                     ctypes.c_int),
+            "ts_moe_route_forward": ([vp, i32, i32, vp, i32, f32, vp, vp, i32, i32, pe, pe, vp, vp,
+                                      vp, vp, vp, vp, sz, i32, vp], ctypes.c_int),
             "ts_moe_device_status": ([vp, ctypes.POINTER(i32), vp], ctypes.c_int),
             "ts_moe_forward_noalloc": ([vp, i32, i32, pe, vp, vp, i32, pe, vp, vp, vp],
                                        ctypes.c_int),
@@ -279,6 +281,32 @@ def forward(x, ex: Experts, idx, w, shared: Experts | None = None, want_f32=Fals
                                     _ptr(y), _ptr(y32), _ptr(ws), ws.numel(), PATH[path],
                                     _stream(stream)))
     return y, y32
+
+
+def route_forward(x, W_r, k, ex: Experts, mode="softmax_k", router_bias=None, per_expert_scale=None,
+                  rmsnorm=False, eps=1e-6, shared: Experts | None = None, want_f32=False, ws=None,
+                  path="auto", out=None, stream=None):
+    """router_route + forward in one call (ts_moe_route_forward): returns (y, y_f32, idx, w).
+    For decode batches on the block-scaled kernels the router launch also does their prep."""
+    import torch
+    T, H = x.shape
+    adt = {torch.float16: "f16", torch.bfloat16: "bf16"}[x.dtype]
+    if ws is None:
+        ws = alloc_workspace(T, k, ex, shared, device=x.device)
+    if out is None:
+        y = torch.empty_like(x)
+        y32 = torch.empty((T, H), dtype=torch.float32, device=x.device) if want_f32 else None
+        idx = torch.empty((T, k), dtype=torch.int32, device=x.device)
+        w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+        xn = torch.empty_like(x) if rmsnorm else None
+    else:
+        y, y32, idx, w, xn = out
+    check(lib().ts_moe_route_forward(_ptr(x), ADT[adt], T, _ptr(W_r), int(rmsnorm), eps,
+                                     _ptr(router_bias), _ptr(per_expert_scale), k, MODE[mode],
+                                     ctypes.byref(ex.c), None if shared is None else ctypes.byref(shared.c),
+                                     _ptr(xn), _ptr(idx), _ptr(w), _ptr(y), _ptr(y32), _ptr(ws),
+                                     ws.numel(), PATH[path], _stream(stream)))
+    return y, y32, idx, w
 
 
 def forward_noalloc(x, ex: Experts, idx, w, shared: Experts | None = None, want_f32=False,

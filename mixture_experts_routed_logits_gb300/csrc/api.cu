@@ -167,7 +167,7 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
 // phase 2 (down -> e, slot-ordered combine -> y).
 ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int32_t* idx,
                       const float* w, int k, const ts_moe_experts* shared, void* y, float* y_f32,
-                      unsigned char* W, const WsLayout& L, cudaStream_t st);
+                      unsigned char* W, const WsLayout& L, cudaStream_t st, bool prep_done);
 
 ts_status launch_gemv_checked(const GemvArgs& a, cudaStream_t st, const char* what) {
     const int sms = num_sms_current();
@@ -179,7 +179,7 @@ ts_status launch_gemv_checked(const GemvArgs& a, cudaStream_t st, const char* wh
 
 ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int32_t* idx,
                       const float* w, int k, const ts_moe_experts* shared, void* y, float* y_f32,
-                      unsigned char* W, const WsLayout& L, cudaStream_t st) {
+                      unsigned char* W, const WsLayout& L, cudaStream_t st, bool prep_done) {
     const int sms = num_sms_current();
     if (sms <= 0) return fail(TS_ERR_CUDA, "ts_moe_forward: no CUDA device");
     int* status = reinterpret_cast<int*>(W + L.status);
@@ -215,7 +215,8 @@ ts_status forward_mxd(const void* x, int T, const ts_moe_experts* ex, const int3
     M.status = status;
     M.stall = g_wait_test;
     g_wait_test = 0;
-    cudaError_t e = launch_mxd_prep(M, st);
+    // the prep launch (x image, counters), unless the router launch already did its work
+    cudaError_t e = prep_done ? cudaSuccess : launch_mxd_prep(M, st);
     if (e == cudaSuccess) e = phase_mark(0, st);
     if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled decode prep");
     if (shared) {
@@ -333,6 +334,26 @@ ts_status ts_moe_pack_mx(int32_t pair, int32_t nmat, int32_t R, int32_t K, const
     return TS_OK;
 }
 
+// argument checks of the router's x / W_r path (ts_moe_router_route, ts_moe_route_forward)
+static ts_status check_router_args(const RouteArgs& a, const char* what) {
+    if (a.adt != TS_DT_F16 && a.adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, a.adt);
+    if (a.H <= 0 || a.H % kBlockK) return fail(TS_ERR_UNSUPPORTED, "%s: H=%d must be a positive multiple of 32", what, a.H);
+    if (a.H > 12288) return fail(TS_ERR_UNSUPPORTED, "%s: H=%d above 12288", what, a.H);
+    if (a.rmsnorm != 0 && a.rmsnorm != 1) return fail(TS_ERR_INVALID_ARG, "%s: rmsnorm must be 0 or 1", what);
+    if (a.T > 0 && (!a.x || !a.Wr)) return fail(TS_ERR_INVALID_ARG, "%s: x or W_r is NULL", what);
+    if (!aligned(a.Wr, 16)) return fail(TS_ERR_INVALID_ARG, "%s: W_r must be 16-byte aligned", what);
+    if (a.T > 0 && a.rmsnorm && !a.xn_out) return fail(TS_ERR_INVALID_ARG, "%s: rmsnorm needs xn_out", what);
+    if (!(a.eps >= 0.0f)) return fail(TS_ERR_INVALID_ARG, "%s: eps must be >= 0", what);
+    if (a.T < 0) return fail(TS_ERR_INVALID_ARG, "%s: T=%d < 0", what, a.T);
+    if (a.E < 1 || a.E > kMaxExperts)
+        return fail(TS_ERR_UNSUPPORTED, "%s: E=%d outside 1..%d", what, a.E, kMaxExperts);
+    if (a.k < 1 || a.k > a.E) return fail(TS_ERR_INVALID_ARG, "%s: k=%d outside 1..E=%d", what, a.k, a.E);
+    if (a.mode < 0 || a.mode > 2) return fail(TS_ERR_INVALID_ARG, "%s: bad mode %d", what, a.mode);
+    if (a.mode == MODE_SOFTMAX_K_SCALED && !a.scale)
+        return fail(TS_ERR_INVALID_ARG, "%s: SOFTMAX_K_SCALED needs per_expert_scale", what);
+    return TS_OK;
+}
+
 static ts_status route_common(RouteArgs& a, cudaStream_t st, const char* what) {
     if (a.T < 0) return fail(TS_ERR_INVALID_ARG, "%s: T=%d < 0", what, a.T);
     if (a.E < 1 || a.E > kMaxExperts)
@@ -431,12 +452,13 @@ size_t ts_moe_workspace_size(int32_t T, int32_t k, const ts_moe_experts* ex,
     return need;
 }
 
-ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
+// The forward; with `fold` (ts_moe_route_forward) the router runs first, and does the decode
+// kernels' prep as well when they take the call.
+static ts_status forward_impl(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
                               const int32_t* idx, const float* w, int32_t k,
                               const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
-                              size_t ws_bytes, int32_t path, void* stream) {
-    g_err.clear();
-    const char* what = "ts_moe_forward";
+                              size_t ws_bytes, int32_t path, void* stream, RouteArgs* fold) {
+    const char* what = fold ? "ts_moe_route_forward" : "ts_moe_forward";
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (adt != TS_DT_F16 && adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, adt);
     if (T < 0) return fail(TS_ERR_INVALID_ARG, "%s: T=%d < 0", what, T);
@@ -490,7 +512,17 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     int32_t* inv = reinterpret_cast<int32_t*>(W + L.inv);
 
     cudaError_t e = cudaSuccess;
-    if (use_mxd) return forward_mxd(x, T, ex, idx, w, k, shared, y, y_f32, W, L, st);
+    if (fold) {
+        if (use_mxd) {
+            // the router launch also does the decode kernels' prep
+            fold->mxd_xs = W + L.dxs;
+            fold->mxd_cnt = reinterpret_cast<int*>(W + L.dcnt);
+            fold->mxd_ncnt = static_cast<int>(L.dcnt_bytes / 4);
+        }
+        s = route_common(*fold, st, "ts_moe_route_forward: router");
+        if (s != TS_OK) return s;
+    }
+    if (use_mxd) return forward_mxd(x, T, ex, idx, w, k, shared, y, y_f32, W, L, st, fold != nullptr);
     if (use_gemm || static_cast<long long>(T) * k > 512)   // else built inside the GEMV kernels
         e = launch_build_routes(idx, T, ex->E, k, off, perm, inv, status, st);
     if (e == cudaSuccess) e = phase_mark(0, st);
@@ -726,6 +758,47 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
     }
     if ((e = phase_mark(5, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
     return TS_OK;
+}
+
+ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
+                              const int32_t* idx, const float* w, int32_t k,
+                              const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
+                              size_t ws_bytes, int32_t path, void* stream) {
+    g_err.clear();
+    return forward_impl(x, adt, T, ex, idx, w, k, shared, y, y_f32, ws, ws_bytes, path, stream, nullptr);
+}
+
+ts_status ts_moe_route_forward(const void* x, int32_t adt, int32_t T, const void* W_r,
+                               int32_t rmsnorm, float eps, const float* router_bias,
+                               const float* per_expert_scale, int32_t k, int32_t mode,
+                               const ts_moe_experts* ex, const ts_moe_experts* shared,
+                               void* xn_out, int32_t* idx, float* w, void* y, float* y_f32,
+                               void* ws, size_t ws_bytes, int32_t path, void* stream) {
+    g_err.clear();
+    const char* what = "ts_moe_route_forward";
+    if (!ex) return fail(TS_ERR_INVALID_ARG, "%s: experts is NULL", what);
+    RouteArgs a{};
+    a.x = x;
+    a.Wr = W_r;
+    a.bias = router_bias;
+    a.scale = per_expert_scale;
+    a.xn_out = xn_out;
+    a.idx = idx;
+    a.w = w;
+    a.T = T;
+    a.H = ex->H;
+    a.E = ex->E;
+    a.k = k;
+    a.mode = mode;
+    a.adt = adt;
+    a.rmsnorm = rmsnorm;
+    a.eps = eps;
+    ts_status s = check_router_args(a, what);
+    if (s != TS_OK) return s;
+    if (T > 0 && (!idx || !w)) return fail(TS_ERR_INVALID_ARG, "%s: idx/w output is NULL", what);
+    // the experts read the normalised rows when the router normalises
+    return forward_impl(rmsnorm ? xn_out : x, adt, T, ex, idx, w, k, shared, y, y_f32, ws, ws_bytes,
+                        path, stream, &a);
 }
 
 ts_status ts_moe_forward(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,

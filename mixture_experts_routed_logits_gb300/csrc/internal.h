@@ -39,6 +39,12 @@ struct RouteArgs {
     float* w;               // [T][k]
     int T, H, E, k, mode, adt, rmsnorm;
     float eps;
+    // the block-scaled decode kernels' prep, folded into the router launch (nullptr: none): the
+    // token rows (after the RMSNorm, when on) split into their x image, rows T..7 zeroed, and the
+    // decode counters zeroed (T <= 8, bf16, H <= 4096)
+    uint8_t* mxd_xs;
+    int* mxd_cnt;
+    int mxd_ncnt;
 };
 cudaError_t launch_router(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off,

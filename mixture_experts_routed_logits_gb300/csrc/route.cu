@@ -15,33 +15,14 @@
 // on the device, so the whole layer is one asynchronous stream of kernels.
 #include <algorithm>
 
-#include "common.cuh"
+#include "mx_common.cuh"
+#include "route_common.cuh"
 
 namespace tsmoe {
 
 namespace {
 
 constexpr int kRouterWarps = 8;   // warps per CTA
-
-
-// Order-preserving map of an f32 to u32 (larger float -> larger integer); -0 folds to +0 so
-// that equal keys tie and fall back to the expert id, as the f32 comparison does.
-__device__ __forceinline__ uint32_t mono_u32(float v) {
-    const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Key for a max-reduction: value first, then the LOWER expert id wins a tie.
-__device__ __forceinline__ uint64_t sel_key(float v, int e) {
-    return (static_cast<uint64_t>(mono_u32(v)) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
-}
-
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
-    uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
-    lo = __shfl_xor_sync(0xffffffffu, lo, o);
-    hi = __shfl_xor_sync(0xffffffffu, hi, o);
-    return (static_cast<uint64_t>(hi) << 32) | lo;
-}
 
 // Router layout.  A CTA takes a tile of `tt` tokens and a group of `ec` experts; the `cl` expert
 // groups of a token tile form one thread-block cluster, so a decode batch of a few tokens still
@@ -256,6 +237,75 @@ router_kernel(RouteArgs a, RouterPlan p) {
             }
             __syncthreads();
         }
+        if (a.mxd_xs) {
+            // ---- the block-scaled decode kernels' prep (their x image and counters), folded in
+            // while the router rows are in flight: each token row is split into two e4m3 terms
+            // under one scale, 2^s with s = floor(log2 max|x_t|) - 7; the CTAs of the cluster
+            // take its 16-column chunks in turn (the image holds the K stages [KG][16 rows][128
+            // B] as the decode kernel's shared memory holds them, 128-byte swizzle, then the
+            // scale atom of the 16 rows) ----
+            const int KG = (H + 127) / 128;
+            unsigned char* atom = a.mxd_xs + static_cast<size_t>(KG) * kMxdBStage;
+            for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.mxd_ncnt; i += gridDim.x * blockDim.x)
+                a.mxd_cnt[i] = 0;
+            __shared__ float red[kRouterWarps];
+            for (int q = 0; q < ntok; ++q) {
+                const int t = t0 + q;
+                const float* xq = xs + static_cast<size_t>(q) * H;
+                float mx = 0.0f;
+                for (int j = threadIdx.x; j < H; j += blockDim.x) mx = fmaxf(mx, fabsf(xq[j]));
+                mx = warp_max(mx);
+                if (lane == 0) red[warp] = mx;
+                __syncthreads();
+                mx = red[0];
+#pragma unroll
+                for (int i = 1; i < kRouterWarps; ++i) mx = fmaxf(mx, red[i]);
+                __syncthreads();
+                const int se = mx_scale_exp(mx);
+                const float inv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);
+                for (int c = static_cast<int>(rank) + p.cl * threadIdx.x; c < KG * 8; c += p.cl * blockDim.x) {
+                    uint32_t q1[4] = {0u, 0u, 0u, 0u}, q2[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) {
+                        const int col = c * 16 + 2 * h;
+                        const float f0 = col < H ? xq[col] : 0.0f, f1 = col + 1 < H ? xq[col + 1] : 0.0f;
+                        uint32_t t1, t2;
+                        mx_split2(__fmul_rn(f0, inv), __fmul_rn(f1, inv), t1, t2);
+                        q1[h >> 1] |= (t1 & 0xFFFFu) << (16 * (h & 1));
+                        q2[h >> 1] |= (t2 & 0xFFFFu) << (16 * (h & 1));
+                    }
+                    unsigned char* sx = a.mxd_xs + static_cast<size_t>(c >> 3) * kMxdBStage;
+                    const int cc = c & 7;
+                    *reinterpret_cast<uint4*>(sx + t * 128 + ((cc ^ t) << 4)) = make_uint4(q1[0], q1[1], q1[2], q1[3]);
+                    *reinterpret_cast<uint4*>(sx + (8 + t) * 128 + ((cc ^ t) << 4)) = make_uint4(q2[0], q2[1], q2[2], q2[3]);
+                }
+                if (rank == 0 && threadIdx.x == 0) {
+                    // rows t (2^s) and 8 + t (2^(s-4)) of the atom; rows 16..31 zero
+                    const uint32_t w0 = static_cast<uint32_t>(se + 127) * 0x01010101u;
+                    *reinterpret_cast<uint4*>(atom + 16 * t) = make_uint4(w0, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(atom + 16 * (8 + t)) = make_uint4(w0 - 0x04040404u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(atom + 16 * (16 + t)) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(atom + 16 * (24 + t)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            if (blockIdx.x == 0) {
+                // the token slots past T: zero rows, and the scale atoms a zero row gets (s = 0)
+                const int nz = (kMxdTokens - a.T) * KG * 16;
+                for (int u = threadIdx.x; u < nz; u += blockDim.x) {
+                    const int t = a.T + u / (KG * 16), r = u % (KG * 16);
+                    const int kg = r >> 4, row = ((r >> 3) & 1) * 8 + t, chunk = r & 7;
+                    *reinterpret_cast<uint4*>(a.mxd_xs + static_cast<size_t>(kg) * kMxdBStage + row * 128 + chunk * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                const int t = a.T + static_cast<int>(threadIdx.x);
+                if (t < kMxdTokens) {
+                    *reinterpret_cast<uint4*>(atom + 16 * t) = make_uint4(0x7F7F7F7Fu, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(atom + 16 * (8 + t)) = make_uint4(0x7B7B7B7Bu, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(atom + 16 * (16 + t)) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(atom + 16 * (24 + t)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
         for (int st = 0; st < nst; ++st) {
             const int slot = st % p.ns;
             const int rows = min(p.rb, ne - st * p.rb);
@@ -305,73 +355,14 @@ router_kernel(RouteArgs a, RouterPlan p) {
     // ---- step 2: per token (one warp each, cluster rank 0): keys, top-k, weights --------------
     if (rank == 0 && warp < ntok) {
         const int t = t0 + warp;
-        float* key = reinterpret_cast<float*>(rsm + p.scr_off) + static_cast<size_t>(warp) * 4 * E;
-        float* sg = key + E;
-        float* ex = key + 2 * E;
-        int* sel = reinterpret_cast<int*>(key + 3 * E);
-        for (int e = lane; e < E; e += 32) {
+        float* scr = reinterpret_cast<float*>(rsm + p.scr_off) + static_cast<size_t>(warp) * 4 * E;
+        auto logit = [&](int e) {
             const uint32_t owner = static_cast<uint32_t>(e / p.ec);
             const float* src = lg + warp * p.ec + (e - static_cast<int>(owner) * p.ec);
-            const float l = p.cl > 1 ? ld_cluster_f32(src, owner) : *src;
-            if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
-            float b = 0.0f;
-#pragma unroll
-            for (int i = 0; i < kMaxExperts / 32; ++i)
-                if (e == lane + 32 * i) b = bias_r[i];
-            float kv;
-            if (a.mode == MODE_SIGMOID_BIASED) {
-                const float sv = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-                sg[e] = sv;
-                kv = a.bias ? __fadd_rn(sv, b) : sv;
-            } else {
-                kv = a.bias ? __fadd_rn(l, b) : l;
-            }
-            key[e] = kv;
-        }
-        __syncwarp();
-        // top-k by repeated warp arg-max; each lane owns experts lane + 32 i
-        uint64_t own[kMaxExperts / 32];
-#pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-            const int e = lane + 32 * i;
-            own[i] = e < E ? sel_key(key[e], e) : 0ull;
-        }
-        for (int s = 0; s < k; ++s) {
-            uint64_t best = 0ull;
-#pragma unroll
-            for (int i = 0; i < kMaxExperts / 32; ++i) best = own[i] > best ? own[i] : best;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const uint64_t other = shfl_xor_u64(best, o);
-                best = other > best ? other : best;
-            }
-            const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
-            if ((e & 31) == lane) {
-#pragma unroll
-                for (int i = 0; i < kMaxExperts / 32; ++i)
-                    if (lane + 32 * i == e) own[i] = 0ull;
-            }
-            if (lane == 0) sel[s] = e;
-        }
-        __syncwarp();
-        if (a.mode == MODE_SIGMOID_BIASED) {
-            for (int s = lane; s < k; s += 32) ex[s] = sg[sel[s]];
-        } else {
-            const float m = key[sel[0]];
-            for (int s = lane; s < k; s += 32) ex[s] = expf(__fsub_rn(key[sel[s]], m));
-        }
-        __syncwarp();
-        float sum = 0.0f;
-        if (lane == 0)
-            for (int s = 0; s < k; ++s) sum = __fadd_rn(sum, ex[s]);   // slot order
-        sum = __shfl_sync(0xffffffffu, sum, 0);
-        const bool aborted = a.x && abort_flag;
-        for (int s = lane; s < k; s += 32) {
-            float wv = __fdiv_rn(ex[s], sum);
-            if (a.mode == MODE_SOFTMAX_K_SCALED) wv = __fmul_rn(wv, a.scale[sel[s]]);
-            a.idx[static_cast<size_t>(t) * k + s] = aborted ? -1 : sel[s];   // -1: a wait gave up
-            a.w[static_cast<size_t>(t) * k + s] = wv;
-        }
+            return p.cl > 1 ? ld_cluster_f32(src, owner) : *src;
+        };
+        route_token_warp(logit, bias_r, E, k, a.mode, a.bias != nullptr, a.scale, scr, t, a.idx, a.w,
+                         a.logits_out, a.x && abort_flag, lane);
     }
     // the other CTAs of the cluster keep their shared memory until rank 0 has read it
     if (p.cl > 1) cluster_sync_all();
