@@ -322,16 +322,23 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     torch.cuda.synchronize()
 
     def step(ly, stream=None):
-        # the whole layer through ts_moe_route_forward: the router, then the experts (the router's
-        # step runs inside the decode kernels' prep launch when they take the call)
+        # the whole layer through ts_moe_route_forward: the router, then the experts (the router
+        # launch also does the decode kernels' prep when they take the call); with the Gemma
+        # sandwich tail, the router then ts_moe_forward_tail (the tail inside the GEMV phase 2
+        # at decode sizes)
         L = ly["L"]
-        moe.route_forward(L["x"], L["Wr"], k, ly["ex"], mode=cfg["mode"], router_bias=L["router_bias"],
-                          per_expert_scale=L["scale"], rmsnorm=cfg["rmsnorm"], shared=ly["sh"],
-                          ws=ly["ws"], path=args.path,
-                          out=(ly["y"], None, ly["idx"], ly["w"], ly["xn"]), stream=stream)
-        if args.gemma_tail:
-            moe.gemma_tail(ly["y"], ly["h1"], ly["xres"], ly["w_post2"], ly["w_post"], 0.5,
-                           stream=stream)
+        if not args.gemma_tail:
+            moe.route_forward(L["x"], L["Wr"], k, ly["ex"], mode=cfg["mode"], router_bias=L["router_bias"],
+                              per_expert_scale=L["scale"], rmsnorm=cfg["rmsnorm"], shared=ly["sh"],
+                              ws=ly["ws"], path=args.path,
+                              out=(ly["y"], None, ly["idx"], ly["w"], ly["xn"]), stream=stream)
+            return
+        moe.router_route(L["x"], L["Wr"], k, mode=cfg["mode"], router_bias=L["router_bias"],
+                         per_expert_scale=L["scale"], rmsnorm=cfg["rmsnorm"],
+                         out=(ly["idx"], ly["w"], ly["xn"], None), stream=stream)
+        moe.forward_tail(ly["xn"] if cfg["rmsnorm"] else L["x"], ly["ex"], ly["idx"], ly["w"], ly["h1"],
+                         ly["xres"], ly["w_post2"], ly["w_post"], 0.5, shared=ly["sh"], ws=ly["ws"],
+                         path=args.path, out=(ly["y"], None), stream=stream)
 
     # ---- CUDA graphs: one per layer, plus a copy with per-phase events -------------------------------
     nph = 8
@@ -376,9 +383,13 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
                and args.path != "gemm_dequant")
     # the decode kernels' prep (x split, counters) done by the router launch
     route_fold = mxd_path
+    # the Gemma tail runs inside the GEMV phase 2 (fused combine), else as a launch of its own
+    tail_fused = bool(args.gemma_tail) and fused_decode and not mxd_path
+    if args.gemma_tail and mxd_path:
+        route_fold = False          # the step is router_route + forward_tail: the prep launches
     n_launch_step = ((2 if route_fold else 3 if mxd_path else 3 if fused_decode else 5 + (1 if gemm_path else 0)
                       + (1 if gemm_path and cfg["fmt"] == "mxfp4" and not mx_path else 0))
-                     + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail else 0))
+                     + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail and not tail_fused else 0))
 
     def timed(K):
         b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -424,7 +435,7 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
         order = [6, 0, 1, 3, 5]
     else:   # GEMV: routed phase 1, shared phase 1, shared phase 2, routed phase 2 (+ combine)
         order = [6, 0, 1] + ([2, 4] if cfg.get("shared_I") else []) + [3, 5]
-    if args.gemma_tail:
+    if args.gemma_tail and not tail_fused:
         order = order + [7]
     samples = {moe.PHASES[j]: [] for j in order}
     for i in range(3 if args.profile else min(args.steps, 50)):

@@ -326,6 +326,22 @@ ts_status ts_moe_gemma_tail(void* y, void* h1, void* x, const void* w_post2, con
 /* Diagnostics.                                                                                */
 /* ------------------------------------------------------------------------------------------ */
 
+/* ts_moe_forward_path followed by ts_moe_gemma_tail(y, h1, xres, w_post2, w_post,
+ * layer_scalar, eps, adt, T, H) in one call, with the same arguments, meaning and results (every
+ * output bit-exact against the two calls; y ends normalised, y_f32 keeps the f32 sum before the
+ * final rounding).  When the streaming GEMV with its fused combine takes the call (decode sizes,
+ * T * k <= 512), the tail runs inside that launch: once every row tile of y is combined, CTA b
+ * runs the tail of tokens b, b + grid, ... (the Gemma-4 batched routed prefill page encodes the
+ * tail right after the fused phase 2).  Otherwise the tail is a launch of its own after the forward.  xres
+ * is the residual stream x of the tail;
+ * checks as ts_moe_forward_path and ts_moe_gemma_tail (H from the experts).               */
+ts_status ts_moe_forward_tail(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
+                              const int32_t* idx, const float* w, int32_t k,
+                              const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
+                              size_t ws_bytes, int32_t path, void* h1, void* xres,
+                              const void* w_post2, const void* w_post, float layer_scalar, float eps,
+                              void* stream);
+
 /* Message of the last failing call on this thread ("" if none).  Valid until the next call. */
 const char* ts_last_error(void);
 

@@ -83,6 +83,8 @@ def lib():
             "ts_moe_set_wait_test": ([i32], ctypes.c_int),
             "ts_moe_set_phase_events": ([ctypes.POINTER(vp), i32], ctypes.c_int),
             "ts_moe_gemma_tail": ([vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, vp], ctypes.c_int),
+            "ts_moe_forward_tail": ([vp, i32, i32, pe, vp, vp, i32, pe, vp, vp, vp, sz, i32, vp, vp, vp,
+                                     vp, f32, f32, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -280,6 +282,30 @@ def forward(x, ex: Experts, idx, w, shared: Experts | None = None, want_f32=Fals
                                     k, None if shared is None else ctypes.byref(shared.c),
                                     _ptr(y), _ptr(y32), _ptr(ws), ws.numel(), PATH[path],
                                     _stream(stream)))
+    return y, y32
+
+
+def forward_tail(x, ex: Experts, idx, w, h1, xres, w_post2, w_post, layer_scalar, eps=1e-6,
+                 shared: Experts | None = None, want_f32=False, ws=None, path="auto", out=None,
+                 stream=None):
+    """forward() then gemma_tail(y, h1, xres, ...) in one call (ts_moe_forward_tail): y comes
+    back normalised, h1 and xres are updated in place; returns (y, y_f32)."""
+    import torch
+    T, H = x.shape
+    k = idx.shape[1]
+    adt = {torch.float16: "f16", torch.bfloat16: "bf16"}[x.dtype]
+    if ws is None:
+        ws = alloc_workspace(T, k, ex, shared, device=x.device)
+    if out is None:
+        y = torch.empty_like(x)
+        y32 = torch.empty((T, H), dtype=torch.float32, device=x.device) if want_f32 else None
+    else:
+        y, y32 = out
+    check(lib().ts_moe_forward_tail(_ptr(x), ADT[adt], T, ctypes.byref(ex.c), _ptr(idx), _ptr(w),
+                                    k, None if shared is None else ctypes.byref(shared.c),
+                                    _ptr(y), _ptr(y32), _ptr(ws), ws.numel(), PATH[path],
+                                    _ptr(h1), _ptr(xres), _ptr(w_post2), _ptr(w_post),
+                                    float(layer_scalar), float(eps), _stream(stream)))
     return y, y32
 
 

@@ -125,7 +125,7 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
         L.s = take(static_cast<size_t>(T) * ex->H * 4);
     }
     L.xs = take(Tk * ex->H * 2);   // activations in route-list order (tensor-core path)
-    L.cmb = take(static_cast<size_t>(ex->H / kRowTile) * 4);   // fused-combine counters
+    L.cmb = take(static_cast<size_t>(ex->H / kRowTile + 1) * 4);   // fused-combine counters + tiles done
     if (ex->fmt == FMT_MXFP4) {      // f16 operands of the MXFP4 tensor-core path
         L.xinv = take(Tk * 4);
         L.hinv = take(Tk * 4);
@@ -453,12 +453,15 @@ size_t ts_moe_workspace_size(int32_t T, int32_t k, const ts_moe_experts* ex,
 }
 
 // The forward; with `fold` (ts_moe_route_forward) the router runs first, and does the decode
-// kernels' prep as well when they take the call.
+// kernels' prep as well when they take the call.  With `tail` (ts_moe_forward_tail) the GEMV
+// phase 2 with the fused combine also runs the Gemma sandwich tail (*tail_done set), else the
+// caller launches it.
 static ts_status forward_impl(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
                               const int32_t* idx, const float* w, int32_t k,
                               const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
-                              size_t ws_bytes, int32_t path, void* stream, RouteArgs* fold) {
-    const char* what = fold ? "ts_moe_route_forward" : "ts_moe_forward";
+                              size_t ws_bytes, int32_t path, void* stream, RouteArgs* fold,
+                              const TailArgs* tail = nullptr, bool* tail_done = nullptr) {
+    const char* what = fold ? "ts_moe_route_forward" : tail ? "ts_moe_forward_tail" : "ts_moe_forward";
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (adt != TS_DT_F16 && adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, adt);
     if (T < 0) return fail(TS_ERR_INVALID_ARG, "%s: T=%d < 0", what, T);
@@ -738,6 +741,14 @@ static ts_status forward_impl(const void* x, int32_t adt, int32_t T, const ts_mo
     g.seed = shared ? reinterpret_cast<const float*>(W + L.s) : nullptr;
     g.y = y;
     g.y_f32 = y_f32;
+    // (the fused tail moves 8 elements at a time: its buffers must be 16-byte aligned)
+    if (fused && tail && !use_gemm && aligned(tail->h1, 16) && aligned(tail->x, 16) &&
+        aligned(tail->w_post2, 16) && aligned(tail->w_post, 16)) {
+        g.tail = *tail;
+        g.tail.y = static_cast<uint16_t*>(y);
+        g.tdone = cmb + ex->H / kRowTile;
+        if (tail_done) *tail_done = true;
+    }
     if (!use_gemm) {
         if ((s = launch_gemv_checked(g, st, "ts_moe_forward: expert phase 2")) != TS_OK) return s;
         if ((e = phase_mark(3, st)) != cudaSuccess) return cuda_fail(e, "ts_moe_forward: phase event");
@@ -766,6 +777,52 @@ ts_status ts_moe_forward_path(const void* x, int32_t adt, int32_t T, const ts_mo
                               size_t ws_bytes, int32_t path, void* stream) {
     g_err.clear();
     return forward_impl(x, adt, T, ex, idx, w, k, shared, y, y_f32, ws, ws_bytes, path, stream, nullptr);
+}
+
+// argument checks of the sandwich tail (ts_moe_gemma_tail, ts_moe_forward_tail)
+static ts_status check_tail_args(const TailArgs& a, const char* what) {
+    if (a.adt != TS_DT_F16 && a.adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, a.adt);
+    if (a.T < 0 || a.H <= 0) return fail(TS_ERR_INVALID_ARG, "%s: bad T=%d / H=%d", what, a.T, a.H);
+    if (a.H % 32 || a.H > kTailMaxH)
+        return fail(TS_ERR_UNSUPPORTED, "%s: H=%d must be a multiple of 32 and at most %d", what, a.H, kTailMaxH);
+    if (a.T == 0) return TS_OK;
+    if (!a.y || !a.h1 || !a.x || !a.w_post2 || !a.w_post) return fail(TS_ERR_INVALID_ARG, "%s: NULL pointer", what);
+    if (a.y == a.h1 || a.y == a.x || a.h1 == a.x)
+        return fail(TS_ERR_INVALID_ARG, "%s: y, h1 and x must be distinct", what);
+    if (!aligned(a.y, 2) || !aligned(a.h1, 2) || !aligned(a.x, 2) || !aligned(a.w_post2, 2) || !aligned(a.w_post, 2))
+        return fail(TS_ERR_INVALID_ARG, "%s: pointers must be 2-byte aligned", what);
+    return TS_OK;
+}
+
+ts_status ts_moe_forward_tail(const void* x, int32_t adt, int32_t T, const ts_moe_experts* ex,
+                              const int32_t* idx, const float* w, int32_t k,
+                              const ts_moe_experts* shared, void* y, float* y_f32, void* ws,
+                              size_t ws_bytes, int32_t path, void* h1, void* xres,
+                              const void* w_post2, const void* w_post, float layer_scalar, float eps,
+                              void* stream) {
+    g_err.clear();
+    const char* what = "ts_moe_forward_tail";
+    if (!ex) return fail(TS_ERR_INVALID_ARG, "%s: experts is NULL", what);
+    TailArgs a{};
+    a.y = static_cast<uint16_t*>(y);
+    a.h1 = static_cast<uint16_t*>(h1);
+    a.x = static_cast<uint16_t*>(xres);
+    a.w_post2 = static_cast<const uint16_t*>(w_post2);
+    a.w_post = static_cast<const uint16_t*>(w_post);
+    a.layer_scalar = layer_scalar;
+    a.eps = eps;
+    a.adt = adt;
+    a.T = T;
+    a.H = ex->H;
+    ts_status s = check_tail_args(a, what);
+    if (s != TS_OK) return s;
+    bool done = false;
+    s = forward_impl(x, adt, T, ex, idx, w, k, shared, y, y_f32, ws, ws_bytes, path, stream, nullptr, &a, &done);
+    if (s != TS_OK || done || T == 0) return s;
+    cudaError_t e = launch_gemma_tail(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = phase_mark(7, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return TS_OK;
 }
 
 ts_status ts_moe_route_forward(const void* x, int32_t adt, int32_t T, const void* W_r,
@@ -830,15 +887,6 @@ ts_status ts_moe_gemma_tail(void* y, void* h1, void* x, const void* w_post2, con
                             void* stream) {
     g_err.clear();
     const char* what = "ts_moe_gemma_tail";
-    if (adt != TS_DT_F16 && adt != TS_DT_BF16) return fail(TS_ERR_INVALID_ARG, "%s: bad adt %d", what, adt);
-    if (T < 0 || H <= 0) return fail(TS_ERR_INVALID_ARG, "%s: bad T=%d / H=%d", what, T, H);
-    if (H % 32 || H > kTailMaxH)
-        return fail(TS_ERR_UNSUPPORTED, "%s: H=%d must be a multiple of 32 and at most %d", what, H, kTailMaxH);
-    if (T == 0) return TS_OK;
-    if (!y || !h1 || !x || !w_post2 || !w_post) return fail(TS_ERR_INVALID_ARG, "%s: NULL pointer", what);
-    if (y == h1 || y == x || h1 == x) return fail(TS_ERR_INVALID_ARG, "%s: y, h1 and x must be distinct", what);
-    if (!aligned(y, 2) || !aligned(h1, 2) || !aligned(x, 2) || !aligned(w_post2, 2) || !aligned(w_post, 2))
-        return fail(TS_ERR_INVALID_ARG, "%s: pointers must be 2-byte aligned", what);
     TailArgs a{};
     a.y = static_cast<uint16_t*>(y);
     a.h1 = static_cast<uint16_t*>(h1);
@@ -850,6 +898,8 @@ ts_status ts_moe_gemma_tail(void* y, void* h1, void* x, const void* w_post2, con
     a.adt = adt;
     a.T = T;
     a.H = H;
+    ts_status s = check_tail_args(a, what);
+    if (s != TS_OK || T == 0) return s;
     cudaError_t e = launch_gemma_tail(a, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = phase_mark(7, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, what);

@@ -27,7 +27,13 @@
 //     [2^14, 2^15)), exact for bf16 inputs in f16's range, undone in f32 after the sum.
 //   * Partial sums of the eight warps are reduced through shared memory in fixed warp order:
 //     results are deterministic run to run.
+//   * Decode calls combine inside phase 2 (the CTA completing a row tile combines it for every
+//     token); with the Gemma sandwich tail requested, the CTAs count the tiles they combined
+//     over the grid, and CTA b, once the count is complete, runs the tail of tokens b, b + grid,
+//     ... (its wait is bounded; it waits only for CTAs that are running or that get an SM as the
+//     launch ahead of this one drains: one CTA per SM, grid = SM count).
 #include "gemv_common.cuh"
+#include "tail_common.cuh"
 
 namespace tsmoe {
 
@@ -260,9 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
         if (lane == 0) c.xinv[t] = inv;
     }
-    // the phase-1 launch clears the combine counters the phase-2 launch will count with
+    // the phase-1 launch clears the combine counters the phase-2 launch will count with (and,
+    // after them, the count of combined tiles)
     if (a.cmb_mode == 1 && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < a.cmb_n; i += blockDim.x) a.cmb_cnt[i] = 0;
+        for (int i = threadIdx.x; i <= a.cmb_n; i += blockDim.x) a.cmb_cnt[i] = 0;
     __syncthreads();
     const int nt = c.misc[0];
     // Phase 2 (one matrix) takes two 16-row tiles per unit, in the slots phase 1 uses for gate
@@ -275,8 +282,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int U = RTu * c.goff[nt];
     const int u0 = static_cast<int>((static_cast<long long>(U) * blockIdx.x) / gridDim.x);
     const int u1 = static_cast<int>((static_cast<long long>(U) * (blockIdx.x + 1)) / gridDim.x);
+    constexpr int kCmbThreads = (kNCW + kReducers) * 32;   // compute + reducer warps
+    const bool tail_on = a.cmb_mode == 2 && a.tail.T > 0;
+
+    // Gemma sandwich tail of tokens blockIdx.x, + gridDim.x, ...: the row's other inputs are
+    // loaded, then the CTA waits (bounded) until every row tile of y is combined, then the compute
+    // and reducer warps finish the row, staged as f32 in the idle weight ring.
+    auto run_tail = [&](int tix) {
+        for (int t = blockIdx.x; t < a.tail.T; t += gridDim.x) {
+            auto ready = [&]() {
+                if (tix == 0) {
+                    int ok = 1;
+                    const long long t0 = clock64();
+                    while (ld_acquire_gpu_s32(a.tdone) < RTu) {
+                        if (clock64() - t0 > (1ll << 31)) {
+                            ok = 0;
+                            report_error(a.status, DEV_ERR_TIMEOUT);
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    c.misc[4] = ok;
+                }
+                named_bar(2, kCmbThreads);
+                const bool ok = c.misc[4] != 0;
+                if (ok) (void)ld_acquire_gpu_s32(a.tdone);   // each thread acquires the rows itself
+                return ok;
+            };
+            if (!gemma_tail_rows_v8(a.tail, t, 1, reinterpret_cast<float*>(c.ring), c.red, tix, kCmbThreads, 2,
+                                    ready))
+                return;
+        }
+    };
+
     if (u0 >= u1) {
         if (early) pdl_wait();  // completes after the launch ahead of it, like every launch
+        if (tail_on && warp != kNCW) run_tail(warp < kNCW ? threadIdx.x : threadIdx.x - 32);
         return;
     }
 
@@ -287,11 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // counters at once (one lane each) and lists the completed tiles, then all compute and
     // reducer warps combine them.
     auto fused_combine = [&]() {
-        constexpr int kCmbThreads = (kNCW + kReducers) * 32;
         named_bar(2, kCmbThreads);                  // combine decision published
-        if (!c.misc[2]) return;
         const int tix = warp < kNCW ? threadIdx.x : threadIdx.x - 32;     // skip the producer warp
-        int jl = 0;
+        if (!c.misc[2]) {
+            if (tail_on) run_tail(tix);         // (its wait runs out: the call has failed)
+            return;
+        }
+        int jl = 0, ncomb = 0;
         for (int ub = u0; ub < u1; ub += 32) {
             if (warp == kNCW + 1) {
                 const int u = ub + lane;
@@ -312,6 +355,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             const int ntile = c.misc[3];
             combine_tiles(a, c.ctile, ntile, TR, tix, kCmbThreads);
             named_bar(2, kCmbThreads);              // tile list consumed
+            ncomb += ntile;
+        }
+        if (tail_on) {
+            // this CTA's combined rows are written (the barrier above): count them (release)
+            if (tix == 0 && ncomb > 0) {
+                __threadfence();
+                asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a.tdone), "r"(ncomb) : "memory");
+            }
+            run_tail(tix);
         }
     };
 
@@ -677,6 +729,12 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
     const int tmax = a.T;                   // tokens per expert never exceed T
     P.p = make_plan(a.fmt, a.K, tmax < 8 ? (tmax > 0 ? tmax : 1) : 8);
     if (P.p.tg < 1) return cudaErrorInvalidValue;
+    const bool tail_on = a.cmb_mode == 2 && a.tail.T > 0;
+    // the tail stages rows of H floats in the weight ring (at least one), 8 elements a thread
+    if (tail_on && (a.tail.H > kTailMaxH || a.tail.H % 8 ||
+                    static_cast<size_t>(a.tail.H) * 4 > static_cast<size_t>(P.p.nstages) * kStageBytes ||
+                    a.tail.H > kTailV * (kNCW + kReducers) * 32 * 8 || !a.tdone))
+        return cudaErrorInvalidValue;
     P.a.tg = P.p.tg;
     void (*kern)(const KParams);
     switch (a.fmt) {

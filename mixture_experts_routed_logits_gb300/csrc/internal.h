@@ -50,6 +50,19 @@ cudaError_t launch_router(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off,
                                 int32_t* perm, int32_t* inv, int* status, cudaStream_t s);
 
+// the Gemma sandwich tail (tail.cu): in place on y, h1, x [T][H] 16-bit
+constexpr int kTailMaxH = 8192;
+struct TailArgs {
+    uint16_t* y;            // routed output -> normalised routed output
+    uint16_t* h1;           // dense branch -> h1 + normalised routed output
+    uint16_t* x;            // residual stream -> (x + normalised h1) * layer_scalar
+    const uint16_t* w_post2;   // [H] bf16 post_feedforward_layernorm_2
+    const uint16_t* w_post;    // [H] bf16 post_feedforward_layernorm
+    float layer_scalar, eps;
+    int adt, T, H;
+};
+cudaError_t launch_gemma_tail(const TailArgs& a, cudaStream_t s);
+
 // ------------------------------------------------------------------------------------------
 // streaming GEMV (decode) path
 // ------------------------------------------------------------------------------------------
@@ -83,6 +96,11 @@ struct GemvArgs {
     void* y;                      // combine: [T][H] adt
     float* y_f32;                 // combine: [T][H] or nullptr
     int stall;                    // test setting: withhold the first weight copy (see api.cu)
+    // the Gemma sandwich tail inside phase 2's fused combine (tail.T > 0; tail.y = y): once
+    // tdone (counted over the grid) reaches the tile count, CTA b runs the tail of tokens b,
+    // b + grid, ...
+    TailArgs tail;
+    int* tdone;                   // row tiles combined (cleared by phase 1 with the counters)
 };
 cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s);
 
@@ -96,18 +114,6 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 
-// the Gemma sandwich tail (tail.cu): in place on y, h1, x [T][H] 16-bit
-constexpr int kTailMaxH = 8192;
-struct TailArgs {
-    uint16_t* y;            // routed output -> normalised routed output
-    uint16_t* h1;           // dense branch -> h1 + normalised routed output
-    uint16_t* x;            // residual stream -> (x + normalised h1) * layer_scalar
-    const uint16_t* w_post2;   // [H] bf16 post_feedforward_layernorm_2
-    const uint16_t* w_post;    // [H] bf16 post_feedforward_layernorm
-    float layer_scalar, eps;
-    int adt, T, H;
-};
-cudaError_t launch_gemma_tail(const TailArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------
 // tensor-core grouped GEMM (prefill) path

@@ -137,3 +137,13 @@ def test_gemma_tail_rejects_bad_arguments(L):
     assert L.ts_moe_gemma_tail(None, *p[1:], f(1.0), f(1e-6), 1, 4, 256, None) == 1
     assert L.ts_moe_gemma_tail(p[0], p[0], *p[2:], f(1.0), f(1e-6), 1, 4, 256, None) == 1   # y == h1
     assert b"distinct" in L.ts_last_error()
+
+
+def test_forward_tail_rejects_bad_arguments(L):
+    """Refused before any device work: no experts, and the tail's own checks (y aliasing h1)."""
+    p = [ctypes.c_void_p(0x1000 + 0x100 * i) for i in range(8)]
+    f = ctypes.c_float
+    args = lambda y, h1: (p[0], 1, 4, None, p[1], p[2], 2, None, y, None, p[3], 1 << 20, 0,
+                          h1, p[5], p[6], p[7], f(1.0), f(1e-6), None)
+    assert L.ts_moe_forward_tail(*args(p[4], p[5])) == 1                        # experts NULL
+    assert b"experts" in L.ts_last_error()
