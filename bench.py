@@ -381,13 +381,16 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # "gemm_dequant" the f16 MMA over dequantised weights (gather, h conversion)
     mx_path = (gemm_path and not mxd_path and cfg["fmt"] == "mxfp4" and cfg["adt"] == "bf16"
                and args.path != "gemm_dequant")
+    # the block-scaled grouped GEMM runs both phases in one launch unless K is split (<= 64 routes)
+    mx_one = mx_path and T * k > 64
     # the decode kernels' prep (x split, counters) done by the router launch
     route_fold = mxd_path
     # the Gemma tail runs inside the GEMV phase 2 (fused combine), else as a launch of its own
     tail_fused = bool(args.gemma_tail) and fused_decode and not mxd_path
     if args.gemma_tail and mxd_path:
         route_fold = False          # the step is router_route + forward_tail: the prep launches
-    n_launch_step = ((2 if route_fold else 3 if mxd_path else 3 if fused_decode else 5 + (1 if gemm_path else 0)
+    n_launch_step = ((2 if route_fold else 3 if mxd_path else 3 if fused_decode else 5 if mx_one
+                      else 5 + (1 if gemm_path else 0)
                       + (1 if gemm_path and cfg["fmt"] == "mxfp4" and not mx_path else 0))
                      + (2 if cfg.get("shared_I") else 0) + (1 if args.gemma_tail and not tail_fused else 0))
 
@@ -431,6 +434,8 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     # [4 shared phase 2], 5 combine, [7 Gemma sandwich tail]
     if mxd_path:   # router (+ prep), [shared phase 1, shared phase 2], both phases + combine
         order = [6] + ([] if route_fold else [0]) + ([2, 4] if cfg.get("shared_I") else []) + [1]
+    elif mx_one:   # router, route list + split, both phases, combine
+        order = [6, 0, 1, 5]
     elif gemm_path:
         order = [6, 0, 1, 3, 5]
     else:   # GEMV: routed phase 1, shared phase 1, shared phase 2, routed phase 2 (+ combine)
@@ -452,6 +457,8 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     if mxd_path:   # the router launch splits x as well; one launch runs both phases
         phases = {("router_and_prep" if n == "router" and route_fold else "prep_x_split" if n == "route_list"
                    else "experts_fused" if n == "experts_phase1" else n): v for n, v in phases.items()}
+    if mx_one:     # one launch runs both phases
+        phases = {("experts_fused" if n == "experts_phase1" else n): v for n, v in phases.items()}
 
     # ---- algorithmic bytes / FLOPs of the dominant kernel (expert phase 1) ---------------------------
     idx_np = layers[0]["idx"].cpu().numpy()
@@ -470,7 +477,7 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
     if cfg.get("shared_I"):
         shared_bytes = 3 * H * cfg["shared_I"] * 2
     step_bytes = p1_bytes + p2_bytes + shared_bytes + E * H * 2 + T * H * 2 * 2 + T * k * H * 4
-    p1_ms = phases["experts_fused" if mxd_path else "experts_phase1"]
+    p1_ms = phases["experts_fused" if (mxd_path or mx_one) else "experts_phase1"]
     routes = T * k
     p1_flop = 2.0 * routes * 2 * I * H
     p2_flop = 2.0 * routes * H * I
@@ -485,14 +492,17 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
                 "traffic": None, "algorithmic_flop": p1_flop, "launch_ms": p1_ms}
         step_tf = (p1_flop + p2_flop) / (ms_max * 1e-3) / 1e12
     else:
-        # the decode kernels run both phases in one launch: its bytes are both phases'
-        k_bytes = p1_bytes + p2_bytes if mxd_path else p1_bytes
+        # the decode kernels, and the block-scaled grouped GEMM above 64 routes, run both phases in
+        # one launch: its bytes are both phases'
+        k_bytes = p1_bytes + p2_bytes if (mxd_path or mx_one) else p1_bytes
         achieved = k_bytes / (p1_ms * 1e-3) / 1e9
         traffic = (captured_traffic("mxd_fused", wl) if mxd_path
                    else None if gemm_path else captured_traffic(f"gemv_{fmt}_phase1", wl))
         roof = {"bound": "hbm",
                 "kernel": ("experts_fused (tcgen05 block-scaled decode kernel: gate/up, down, combine; "
                            "stream-K, cooperative)" if mxd_path else
+                           "experts_fused (tcgen05 block-scaled grouped GEMM: gate/up and down in one "
+                           "cooperative launch, items from one counter)" if mx_one else
                            "experts_phase1 (tcgen05 block-scaled grouped GEMM, MXFP4 gate/up)"
                            if mx_path else
                            "experts_phase1 (tcgen05 grouped GEMM over packed MXFP4, gate/up)"
@@ -539,6 +549,8 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
         "path": ("tcgen05 block-scaled decode kernels (kind::mxf8f6f4, stream-K over every SM, TMA + TMEM; "
                  + ("router launch with the prep folded in, " if route_fold else "prep, ")
                  + "gate/up, down + fused combine)" if mxd_path
+                 else "tcgen05 block-scaled grouped GEMM (kind::mxf8f6f4, TMA + TMEM; gate/up and down in one "
+                      "launch)" if mx_one
                  else "tcgen05 block-scaled grouped GEMM (kind::mxf8f6f4, TMA + TMEM)" if mx_path
                  else "tcgen05 grouped GEMM (TMA + TMEM)" if gemm_path
                  else "gemv (mma.sync m16n8k16 over streamed tiles)"),

@@ -98,6 +98,7 @@ ts_status check_experts(const ts_moe_experts* ex, const char* what, int adt) {
 struct WsLayout {
     size_t status, off, perm, inv, h, e, hs, s, xs, xinv, hinv, h16, cmb, part, tcnt, total;
     size_t xq, xsf, hq, hsf;   // block-scaled path: split activations and their scales
+    size_t hrdy;               // block-scaled path, both phases in one launch: h-ready counters
     size_t dxs, dhs, dpart, dcnt, dcnt_bytes;   // block-scaled decode kernels (T <= 8)
     size_t tcnt_n;        // split-K group counters per phase
     int max_split;        // > 1 when the partials fit (decode sizes)
@@ -135,6 +136,7 @@ WsLayout ws_layout(int T, int k, const ts_moe_experts* ex, const ts_moe_experts*
         L.xsf = take(Tk * mx_sf_row(ex->H));
         L.hq = take(2 * Tk * ex->I);
         L.hsf = take(Tk * mx_sf_row(ex->I));
+        L.hrdy = take((Tk + 1) * 4);   // one per (touched expert, route tile) at most + the item count
         if (T <= kMxdTokens && Tk <= kMxdMaxTouched && k <= kMxdMaxK && ex->H <= kMxdMaxH) {
             // decode kernels: the split x and h images, stream-K partials, and the part /
             // row-block counters
@@ -537,7 +539,11 @@ static ts_status forward_impl(const void* x, int32_t adt, int32_t T, const ts_mo
         const int Tk = T * k;
         uint8_t* xq = W + L.xq;
         uint8_t* xsf = W + L.xsf;
-        e = launch_mx_split_rows(static_cast<const uint16_t*>(x), perm, k, ex->H, Tk, xq, xsf, st);
+        // both phases in one launch unless K is split (decode-sized calls)
+        const bool one_launch = L.max_split <= 1;
+        int* hrdy = reinterpret_cast<int*>(W + L.hrdy);
+        e = launch_mx_split_rows(static_cast<const uint16_t*>(x), perm, k, ex->H, Tk, xq, xsf, hrdy,
+                                 one_launch ? Tk + 1 : 0, st);
         if (e == cudaSuccess) e = phase_mark(0, st);
         if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: activation split");
         MxArgs M{};
@@ -562,25 +568,33 @@ static ts_status forward_impl(const void* x, int32_t adt, int32_t T, const ts_mo
         M.max_split = L.max_split;
         M.part = L.max_split > 1 ? reinterpret_cast<float*>(W + L.part) : nullptr;
         M.cnt = L.max_split > 1 ? reinterpret_cast<int*>(W + L.tcnt) : nullptr;
-        if (L.max_split > 1) e = cudaMemsetAsync(W + L.tcnt, 0, 2 * L.tcnt_n * 4, st);
-        if (e == cudaSuccess) e = launch_mx_gemm(M, sms, st);
-        if (e == cudaSuccess) e = phase_mark(1, st);
-        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled phase 1");
-        M.phase = 1;
-        M.w = static_cast<const uint8_t*>(ex->down_mx);
-        M.b0 = static_cast<const uint16_t*>(ex->down_b);
-        M.b1 = nullptr;
-        M.R = ex->H;
-        M.K = ex->I;
-        M.bq = W + L.hq;
-        M.bsf = W + L.hsf;
-        M.hq = nullptr;
-        M.hsf = nullptr;
-        M.e_out = reinterpret_cast<float*>(W + L.e);
-        if (L.max_split > 1) M.cnt = reinterpret_cast<int*>(W + L.tcnt) + L.tcnt_n;
-        e = launch_mx_gemm(M, sms, st);
-        if (e == cudaSuccess) e = phase_mark(3, st);
-        if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled phase 2");
+        MxArgs M1 = M;
+        M1.phase = 1;
+        M1.w = static_cast<const uint8_t*>(ex->down_mx);
+        M1.b0 = static_cast<const uint16_t*>(ex->down_b);
+        M1.b1 = nullptr;
+        M1.R = ex->H;
+        M1.K = ex->I;
+        M1.bq = W + L.hq;
+        M1.bsf = W + L.hsf;
+        M1.hq = nullptr;
+        M1.hsf = nullptr;
+        M1.e_out = reinterpret_cast<float*>(W + L.e);
+        if (L.max_split > 1) M1.cnt = reinterpret_cast<int*>(W + L.tcnt) + L.tcnt_n;
+        if (one_launch) {
+            e = launch_mx_fused(M, M1, hrdy, sms, st);
+            if (e == cudaSuccess) e = phase_mark(1, st);
+            if (e == cudaSuccess) e = phase_mark(3, st);
+            if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled phases");
+        } else {
+            e = cudaMemsetAsync(W + L.tcnt, 0, 2 * L.tcnt_n * 4, st);
+            if (e == cudaSuccess) e = launch_mx_gemm(M, sms, st);
+            if (e == cudaSuccess) e = phase_mark(1, st);
+            if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled phase 1");
+            e = launch_mx_gemm(M1, sms, st);
+            if (e == cudaSuccess) e = phase_mark(3, st);
+            if (e != cudaSuccess) return cuda_fail(e, "ts_moe_forward: block-scaled phase 2");
+        }
     } else if (use_gemm) {
         const int sms = num_sms_current();
         if (sms <= 0) return fail(TS_ERR_CUDA, "%s: no CUDA device", what);

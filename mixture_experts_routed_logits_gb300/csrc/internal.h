@@ -199,10 +199,15 @@ struct MxArgs {
     int* cnt;                     // split-K group counters (zero before the launch)
 };
 cudaError_t launch_mx_gemm(const MxArgs& a, int num_sms, cudaStream_t s);
+// both phases in one cooperative launch (a0.phase 0, a1.phase 1, no split K): the CTAs draw
+// items from one counter (hrdy[rows_in]); phase-1 items wait for the h of their (touched expert,
+// route tile), counted in hrdy[0 .. rows_in) (all rows_in + 1 zero before the launch)
+cudaError_t launch_mx_fused(const MxArgs& a0, const MxArgs& a1, int* hrdy, int num_sms, cudaStream_t s);
 // bf16 rows (route-list order, row p = x[perm[p] / k]; perm nullptr: row p = x[p]) split into two
-// e4m3 planes [2][n][K] and e8m0 block scales, words [mx_sf_row(K) / 4][n] of four blocks
+// e4m3 planes [2][n][K] and e8m0 block scales, words [mx_sf_row(K) / 4][n] of four blocks; block
+// 0 also zeroes zero[0 .. nzero)
 cudaError_t launch_mx_split_rows(const uint16_t* x, const int32_t* perm, int k, int K, int n,
-                                 uint8_t* q, uint8_t* sf, cudaStream_t s);
+                                 uint8_t* q, uint8_t* sf, int* zero, int nzero, cudaStream_t s);
 // canonical codes / scales of one matrix (G = 1) or of gate and up (G = 2: codes1/scales1 = up)
 cudaError_t launch_mx_pack(int G, int nmat, int R, int K, const uint8_t* codes0, const uint8_t* scales0,
                            const uint8_t* codes1, const uint8_t* scales1, uint8_t* blob, cudaStream_t s);

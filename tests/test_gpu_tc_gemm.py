@@ -33,7 +33,8 @@ CASES = [
     (5, 300, dict(H=256, I=256, E=4, k=2)),           # > 256 routes per expert: 2+ route tiles
     (1, 20, dict(H=128, I=256, E=8, k=2)),            # f16 weights + f16 activations
     (5, 2048, None),                                  # full Mixtral-8x7B prefill chunk
-    (2, 40, dict(H=512, I=384, E=8, k=4)),            # MXFP4 + clamped SwiGLU + biases
+    (2, 40, dict(H=512, I=384, E=8, k=4)),            # MXFP4 + clamped SwiGLU + biases (one launch)
+    (2, 16, dict(H=512, I=384, E=8, k=4)),            # MXFP4, 64 routes: split K, two launches
     (3, 77, dict(H=640, I=448, E=8, k=4)),            # MXFP4, skewed, partial 128-row blocks
     (3, 512, None),                                   # full gpt-oss prefill micro-batch
     (2, 1, None),                                     # gpt-oss decode T=1 (split K)
