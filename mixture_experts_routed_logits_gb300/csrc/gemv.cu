@@ -202,7 +202,9 @@ __device__ __forceinline__ int block_slot(int w) {
     return static_cast<int>((kSlots >> (4 * w)) & 15u);
 }
 
-template <int FMT>
+// TAIL: the phase-2 launch that also runs the Gemma sandwich tail (its code exists only in that
+// instantiation: compiled into every launch it measured a few per cent slower everywhere).
+template <int FMT, bool TAIL>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ KParams P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const GemvArgs& a = P.a;
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int u0 = static_cast<int>((static_cast<long long>(U) * blockIdx.x) / gridDim.x);
     const int u1 = static_cast<int>((static_cast<long long>(U) * (blockIdx.x + 1)) / gridDim.x);
     constexpr int kCmbThreads = (kNCW + kReducers) * 32;   // compute + reducer warps
-    const bool tail_on = a.cmb_mode == 2 && a.tail.T > 0;
+    constexpr bool tail_on = TAIL;
 
     // Gemma sandwich tail of tokens blockIdx.x, + gridDim.x, ...: the row's other inputs are
     // loaded, then the CTA waits (bounded) until every row tile of y is combined, then the compute
@@ -738,18 +740,12 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t s) {
     P.a.tg = P.p.tg;
     void (*kern)(const KParams);
     switch (a.fmt) {
-        case FMT_F16: kern = gemv_kernel<FMT_F16>; break;
-        case FMT_BF16: kern = gemv_kernel<FMT_BF16>; break;
-        case FMT_MXFP4: kern = gemv_kernel<FMT_MXFP4>; break;
-        default: kern = gemv_kernel<FMT_INT4>; break;
+        case FMT_F16: kern = tail_on ? gemv_kernel<FMT_F16, true> : gemv_kernel<FMT_F16, false>; break;
+        case FMT_BF16: kern = tail_on ? gemv_kernel<FMT_BF16, true> : gemv_kernel<FMT_BF16, false>; break;
+        case FMT_MXFP4: kern = tail_on ? gemv_kernel<FMT_MXFP4, true> : gemv_kernel<FMT_MXFP4, false>; break;
+        default: kern = tail_on ? gemv_kernel<FMT_INT4, true> : gemv_kernel<FMT_INT4, false>; break;
     }
-    cudaError_t e;
-    switch (a.fmt) {
-        case FMT_F16: e = ensure_smem(gemv_kernel<FMT_F16>, P.p.smem); break;
-        case FMT_BF16: e = ensure_smem(gemv_kernel<FMT_BF16>, P.p.smem); break;
-        case FMT_MXFP4: e = ensure_smem(gemv_kernel<FMT_MXFP4>, P.p.smem); break;
-        default: e = ensure_smem(gemv_kernel<FMT_INT4>, P.p.smem); break;
-    }
+    const cudaError_t e = ensure_smem(kern, P.p.smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(num_sms), dim3(kThreads), P.p.smem, s, P);
 }

@@ -101,6 +101,9 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
     return v;
 }
 
+// PREP: the launch also does the block-scaled decode kernels' prep (a.mxd_xs set; that code
+// exists only in this instantiation)
+template <bool PREP>
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_kernel(RouteArgs a, RouterPlan p) {
     extern __shared__ __align__(128) unsigned char rsm[];
@@ -237,7 +240,7 @@ router_kernel(RouteArgs a, RouterPlan p) {
             }
             __syncthreads();
         }
-        if (a.mxd_xs) {
+        if (PREP) {
             // ---- the block-scaled decode kernels' prep (their x image and counters), folded in
             // while the router rows are in flight: each token row is split into two e4m3 terms
             // under one scale, 2^s with s = floor(log2 max|x_t|) - 7; the CTAs of the cluster
@@ -449,7 +452,8 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
 cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
     const RouterPlan p = router_plan(a.T, a.H, a.E, a.x != nullptr);
-    cudaError_t e = ensure_smem(router_kernel, p.smem);
+    auto kern = a.mxd_xs ? router_kernel<true> : router_kernel<false>;
+    cudaError_t e = ensure_smem(kern, p.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ntiles * p.cl);
@@ -465,7 +469,7 @@ cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
     at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, router_kernel, a, p);
+    return cudaLaunchKernelEx(&cfg, kern, a, p);
 }
 
 cudaError_t launch_build_routes(const int32_t* idx, int T, int E, int k, int32_t* off,
