@@ -497,6 +497,7 @@ def measure(cfg_id, T, args, ws, rank, local, hbm_peak, bf16_sust, peak_src, min
         k_bytes = p1_bytes + p2_bytes if (mxd_path or mx_one) else p1_bytes
         achieved = k_bytes / (p1_ms * 1e-3) / 1e9
         traffic = (captured_traffic("mxd_fused", wl) if mxd_path
+                   else captured_traffic("mx_fused", wl) if mx_one
                    else None if gemm_path else captured_traffic(f"gemv_{fmt}_phase1", wl))
         roof = {"bound": "hbm",
                 "kernel": ("experts_fused (tcgen05 block-scaled decode kernel: gate/up, down, combine; "
