@@ -35,6 +35,9 @@ CASES = [
     (5, 2048, None),                                  # full Mixtral-8x7B prefill chunk
     (2, 40, dict(H=512, I=384, E=8, k=4)),            # MXFP4 + clamped SwiGLU + biases (one launch)
     (2, 16, dict(H=512, I=384, E=8, k=4)),            # MXFP4, 64 routes: split K, two launches
+    (2, 17, dict(H=512, I=384, E=8, k=4)),            # 68 routes: both phases in one launch
+    (2, 40, dict(H=256, I=256, E=128, k=8)),          # one launch, many experts with a tile or two
+    (3, 96, dict(H=1024, I=640, E=16, k=4)),          # one launch, skewed, ragged row blocks
     (3, 77, dict(H=640, I=448, E=8, k=4)),            # MXFP4, skewed, partial 128-row blocks
     (3, 512, None),                                   # full gpt-oss prefill micro-batch
     (2, 1, None),                                     # gpt-oss decode T=1 (split K)
@@ -103,6 +106,19 @@ def test_gemm_and_gemv_paths_agree(case):
     a32, b32 = ya32.double().cpu().numpy(), yb32.double().cpu().numpy()
     rel = np.linalg.norm(a32 - b32) / np.linalg.norm(a32)
     assert np.abs(a32 - b32).max() <= 2e-2 and rel <= 1e-3, rel
+
+
+def test_mx_one_launch_deterministic():
+    """Both block-scaled phases in one launch hand items out from a counter, so a run's items
+    land on other CTAs than the last run's: the outputs must not change."""
+    moe = _moe()
+    L, D = _make(3, 160, dict(H=512, I=512, E=32, k=4))
+    ex, _ = gpu_layer(D)
+    idx, w, _, _ = moe.router_route(D["x"], D["Wr"], 4, router_bias=D["router_bias"])
+    outs = [moe.forward(D["x"], ex, idx, w, want_f32=True, path="gemm")[1].clone() for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
 
 
 def test_tc_gemm_deterministic():
