@@ -46,6 +46,7 @@ SMALL = [
     (4, 8, dict(H=256, I=96, E=16, k=8, shared_I=128)),
     (4, 8, None),                                        # full Gemma-style layer
     (4, 3, dict(H=128, I=64, E=4, k=1, shared_I=64)),
+    (4, 4, dict(H=1024, I=256, E=32, k=8, shared_I=128)),  # phase-2 units of two row tiles
     (5, 9, dict(H=256, I=512, E=8, k=2)),
     (5, 8, dict(H=4096, I=14336, E=8, k=2)),             # Mixtral-8x7B decode, 8 tokens
     (2, 8, dict(H=256, I=128, E=256, k=8)),              # the largest expert count (256)
@@ -122,6 +123,15 @@ def test_forward_parity(case):
                                   (5, 256, dict(H=128, I=256, E=8, k=2)),
                                   (5, 257, dict(H=128, I=256, E=8, k=2))], ids=_ids)
 def test_gemv_path_on_both_sides_of_the_fused_route_list(case):
+    _forward_parity(case, "gemv")
+
+
+# MXFP4 through the GEMV with enough phase-2 work that each unit takes two 16-row tiles (at
+# least eight units per CTA), at sizes the oracle checks element by element; the second case
+# has a down projection of two 32-column blocks
+@pytest.mark.parametrize("case", [(2, 4, dict(H=2048, I=256, E=32, k=8)),
+                                  (2, 6, dict(H=2048, I=64, E=64, k=8))], ids=_ids)
+def test_gemv_phase2_units_of_two_row_tiles(case):
     _forward_parity(case, "gemv")
 
 
