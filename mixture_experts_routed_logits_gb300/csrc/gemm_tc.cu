@@ -22,8 +22,9 @@
 //     route-list order.  Phase 2: two accumulators cover 256 rows of the down projection;
 //     epilogue adds the bias and stores f32 expert outputs by route id for the combine.
 //   * Warp roles: warp 0 = TMA producer (3-stage ring of 64 KB), warp 1 = MMA issuer (one
-//     thread, tcgen05.mma kind::f16, 128B-swizzled K-major smem descriptors), warps 2-5 =
-//     epilogue (tcgen05.ld of their TMEM lane quarter).  Every mbarrier wait is bounded.
+//     thread, tcgen05.mma kind::f16, 128B-swizzled K-major smem descriptors), the rest =
+//     epilogue (tcgen05.ld of their TMEM lane quarter, warp w taking quarter w % 4): warps 2-25
+//     for 16-bit weights, 2-5 for MXFP4.  Every mbarrier wait is bounded.
 //   * MXFP4 weights (QUANT variant): the producer bulk-copies the packed e2m1 tiles (with their
 //     e8m0 block scales) into a staging area of each stage; sixteen dequant warps turn them
 //     into f16 (hardware e2m1x2 -> f16x2 convert, times the block scale, exact while the scale
@@ -47,6 +48,12 @@ constexpr int kBK = 64;                          // K elements per stage (128 by
 constexpr int kATile = kBM * kBK * 2;            // 16 KB
 constexpr int kBBox = 64 * kBK * 2;              // 8 KB: one 64-row TMA box of activations
 constexpr int kThreads = 192;
+// 16-bit weights: 24 epilogue warps (six per TMEM lane quarter, 16-column chunks dealt in
+// turn) drain the single accumulator set of a 256-route tile while the tensor pipe waits for
+// it (the activation and the stores of 64K h values per gate/up item); measured on the
+// Mixtral prefill chunk, gate/up launch: 4 warps 937 us, 8 782, 16 712, 24 685
+constexpr int kEpiWarps16 = 24;
+constexpr int kThreads16 = (2 + kEpiWarps16) * 32;
 // QUANT variant: a packed slot holds the B boxes and two 8-row-tile x 2-block packed tiles
 constexpr int kPackBlk = 272;
 constexpr int kStaging = 2 * 8 * 2 * kPackBlk;             // 8704 B
@@ -89,7 +96,7 @@ struct SmemTail {
 };
 
 template <bool QUANT>
-__global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads, 1)
+__global__ void __launch_bounds__(QUANT ? kThreadsQ : kThreads16, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const TcLayout& Ly = P.ly;
@@ -144,7 +151,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tl->tfull[b], 1);
-            mbar_init(&tl->tempty[b], 4);
+            mbar_init(&tl->tempty[b], QUANT ? 4 : kEpiWarps16);
         }
         fence_mbar_init();
     }
@@ -351,6 +358,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         // =================================== epilogue ==========================================
         const int q = warp & 3;                     // TMEM lane quarter this warp may access
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        // warps per lane quarter, and which of them this is: 16-column chunks alternate
+        const int nh = QUANT ? 1 : kEpiWarps16 / 4;
+        const int hw = QUANT ? 0 : (warp - 2) >> 2;
         const int Tk = a.rows_in;
         int n_item = 0;
         for (int i = blockIdx.x; i < items; i += gridDim.x, ++n_item) {
@@ -387,7 +397,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             uint16_t* hout = static_cast<uint16_t*>(a.out);
             float* eout = static_cast<float*>(a.out);
             if (S == 1) {
-                for (int c0 = 0; c0 < N; c0 += 16) {
+                for (int c0 = 16 * hw; c0 < N; c0 += 16 * nh) {
                     float d0[16], d1[16];
                     tmem_ld16_pair(tqs + c0, tqs + acc1 + c0, d0, d1);
                     if (a.phase == 0) {
@@ -426,7 +436,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             }
             // split K: park this part's accumulators, the group's last part finishes
             float* part = a.part;
-            for (int c0 = 0; c0 < N; c0 += 16) {
+            for (int c0 = 16 * hw; c0 < N; c0 += 16 * nh) {
                 float d0[16], d1[16];
                 tmem_ld16_pair(tqs + c0, tqs + acc1 + c0, d0, d1);
 #pragma unroll
@@ -441,15 +451,16 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tl->tempty[tb]);   // this set is free again
-            // each warp owns its 32-row slice: one counter per (group, slice), so no barrier
-            // between the epilogue warps is needed
+            // the warps of a lane quarter own its 32-row slice: one counter per (group, slice),
+            // counting every part's warps, so no barrier between the epilogue warps is needed;
+            // the last to arrive sums every column of the slice
             __threadfence();
             __syncwarp();
             int last = 0;
             if (lane == 0) {
                 const int slot = (i / S) * 4 + q;
                 const int prev = atomicAdd(a.cnt + slot, 1);
-                last = (prev + 1 == S);
+                last = (prev + 1 == S * nh);
                 if (last) a.cnt[slot] = 0;               // ready for the next call
             }
             if (__shfl_sync(0xffffffffu, last, 0) == 0) continue;
@@ -698,7 +709,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, int num_sms, cudaStream_t s) {
     } else {
         e = ensure_smem(tc_gemm_kernel<false>, smem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(tc_gemm_kernel<false>, dim3(num_sms), dim3(kThreads), smem, s, P);
+        return launch_pdl(tc_gemm_kernel<false>, dim3(num_sms), dim3(kThreads16), smem, s, P);
     }
     return cudaGetLastError();
 }

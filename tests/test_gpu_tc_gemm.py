@@ -33,6 +33,8 @@ CASES = [
     (5, 300, dict(H=256, I=256, E=4, k=2)),           # > 256 routes per expert: 2+ route tiles
     (1, 20, dict(H=128, I=256, E=8, k=2)),            # f16 weights + f16 activations
     (5, 2048, None),                                  # full Mixtral-8x7B prefill chunk
+    (5, 512, dict(H=1024, I=2048, E=8, k=2)),         # 256-route tiles, 32 down items on 152 SMs
+    (5, 600, dict(H=1024, I=2048, E=4, k=2)),         # two route tiles per expert
     (2, 40, dict(H=512, I=384, E=8, k=4)),            # MXFP4 + clamped SwiGLU + biases (one launch)
     (2, 16, dict(H=512, I=384, E=8, k=4)),            # MXFP4, 64 routes: split K, two launches
     (2, 17, dict(H=512, I=384, E=8, k=4)),            # 68 routes: both phases in one launch
@@ -91,7 +93,8 @@ def test_tc_gemm_parity(case, path):
 
 
 @pytest.mark.parametrize("case", [(5, 8, dict(H=512, I=1024, E=8, k=2)), (5, 64, dict(H=256, I=512, E=8, k=2)),
-                                  (2, 8, dict(H=2880, I=2880, E=32, k=4)), (3, 48, dict(H=512, I=512, E=8, k=4))],
+                                  (2, 8, dict(H=2880, I=2880, E=32, k=4)), (3, 48, dict(H=512, I=512, E=8, k=4)),
+                                  (5, 300, dict(H=1024, I=1024, E=8, k=2))],   # 256-route tiles
                          ids=_ids)
 def test_gemm_and_gemv_paths_agree(case):
     moe = _moe()
@@ -121,13 +124,18 @@ def test_mx_one_launch_deterministic():
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
 
 
-def test_tc_gemm_deterministic():
+@pytest.mark.parametrize("T,shapes", [(96, dict(H=256, I=512, E=8, k=2)),
+                                      (512, dict(H=1024, I=2048, E=8, k=2))])   # 256-route tiles
+def test_tc_gemm_deterministic(T, shapes):
+    """Repeated calls give the same bits."""
     moe = _moe()
-    L, D = _make(5, 96, dict(H=256, I=512, E=8, k=2))
+    L, D = _make(5, T, shapes)
     ex, _ = gpu_layer(D)
     idx, w, _, _ = moe.router_route(D["x"], D["Wr"], 2)
-    outs = [moe.forward(D["x"], ex, idx, w, want_f32=True, path="gemm")[1].clone() for _ in range(3)]
+    ws = moe.alloc_workspace(T, 2, ex, None)
+    outs = [moe.forward(D["x"], ex, idx, w, want_f32=True, ws=ws, path="gemm")[1].clone() for _ in range(3)]
     torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
 
