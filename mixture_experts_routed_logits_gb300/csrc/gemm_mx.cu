@@ -35,7 +35,8 @@
 //     GB300), so the copies are few, large, and issued from two warps.
 //   * Warps: 0 weight producer, 7 scale + activation producer (each also prefetches its share
 //     of a later stage into L2), 1 MMA issuer (one thread, only MMAs: ~88 clocks each for this
-//     kind up to N = 128), 2-5 epilogue (one TMEM lane quarter each), 6 builds the activation
+//     kind up to N = 128), 2-5 and 8-11 epilogue (two per TMEM lane quarter, alternate groups
+//     of 8 route columns), 6 builds the activation
 //     scale atoms and copies every stage's scale atoms into TMEM (tcgen05.cp, committed to the
 //     stage's scale barrier).  Every mbarrier wait is bounded.
 //   * Above 64 routes one cooperative launch runs both phases (gate/up, bias, clamped SwiGLU and
@@ -59,10 +60,12 @@ constexpr int kMxAtx = 8192;          // transaction bytes of one A box (the pac
 constexpr int kMxAtom = 512;          // scale atom: 128 rows x 4 blocks
 constexpr int kMxNbMax = 56;          // routes per tile with two accumulator sets
 constexpr int kMxNbMax1 = 112;        // routes per tile with one accumulator set
-constexpr int kMxThreads = 256;      // 8 warps: see the roles in the file header
+constexpr int kMxEpiWarps = 8;        // epilogue warps: 2-5 and 8.., kMxEpiWarps / 4 per lane quarter
+constexpr int kMxThreads = (kMxEpiWarps + 4) * 32;   // see the roles in the file header
+static_assert(kMxEpiWarps % 4 == 0, "whole TMEM lane quarters");
 constexpr int kMxMaxSlots = 6;
 constexpr int kMxQ = 8;               // item queue entries (two-phase launch)
-constexpr int kMxQReaders = 7;        // roles reading each entry: warps 7, 6, 1 and 2-5
+constexpr int kMxQReaders = 3 + kMxEpiWarps;   // roles reading each entry: warps 7, 6, 1, epilogue
 
 struct MxLayout {
     int nb;               // routes per tile at most (multiple of 8); the MMA's N is 2 nb
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) tc_mx_kernel(const __grid_const
     const int NS = Ly.nslot;
     const int NMAX = 2 * Ly.nb;                       // accumulator columns per matrix
     const int Tk = a0.rows_in;
-    const int hdone = P.hrdy ? gA.MB * 4 : 0;         // phase-0 slices of one (expert, tile)
+    const int hdone = P.hrdy ? gA.MB * kMxEpiWarps : 0;   // phase-0 slices of one (expert, tile)
 
     if (threadIdx.x == 0) {
         int nt = 0, acc0 = 0, acc1 = 0, tacc = 0;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) tc_mx_kernel(const __grid_const
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tl->tfull[b], 1);
-            mbar_init(&tl->tempty[b], 4);
+            mbar_init(&tl->tempty[b], kMxEpiWarps);
         }
         for (int q = 0; q < kMxQ; ++q) {
             mbar_init(&tl->qfull[q], 1);
@@ -580,6 +583,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) tc_mx_kernel(const __grid_const
     } else {
         // =================================== epilogue ==========================================
         const int q = warp & 3;                     // TMEM lane quarter of this warp
+        // nh warps per quarter (2-5, 8-11, ...) take groups of 8 route columns in turn
+        constexpr int nh = kMxEpiWarps / 4;
+        const int hw = warp < 8 ? 0 : (warp - 4) >> 2;
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16);
         int n_item = 0;
         bool stop = false;
@@ -663,7 +669,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) tc_mx_kernel(const __grid_const
                     }
                 };
                 if (S == 1) {
-                    for (int c0 = 0; c0 < nv; c0 += 8) {
+                    for (int c0 = 8 * hw; c0 < nv; c0 += 8 * nh) {
                         float d0[8], d0b[8], d1[8], d1b[8];
                         tmem_ld8x4(t0 + c0, t0 + tw + c0, t1 + c0, t1 + tw + c0, d0, d0b, d1, d1b);
 #pragma unroll
@@ -683,7 +689,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) tc_mx_kernel(const __grid_const
                 }
                 // split K: park this part's sums, the group's last part finishes
                 float* part = a.part;
-                for (int c0 = 0; c0 < nv; c0 += 8) {
+                for (int c0 = 8 * hw; c0 < nv; c0 += 8 * nh) {
                     float d0[8], d0b[8], d1[8], d1b[8];
                     tmem_ld8x4(t0 + c0, t0 + tw + c0, t1 + c0, t1 + tw + c0, d0, d0b, d1, d1b);
 #pragma unroll
@@ -704,7 +710,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) tc_mx_kernel(const __grid_const
                 if (lane == 0) {
                     const int slot = (i / S) * 4 + q;
                     const int prev = atomicAdd(a.cnt + slot, 1);
-                    last = (prev + 1 == S);
+                    last = (prev + 1 == S * nh);            // every part's warps of the quarter
                     if (last) a.cnt[slot] = 0;               // ready for the next call
                 }
                 if (__shfl_sync(0xffffffffu, last, 0) == 0) return true;
