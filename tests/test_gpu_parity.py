@@ -87,6 +87,42 @@ def test_router_bit_exact(case):
     assert np.array_equal(w2.cpu().numpy().view(np.uint32), w.cpu().numpy().view(np.uint32))
 
 
+# Prefill-sized router calls with few experts (more than 64 tokens, at most 16 experts, no RMSNorm)
+# take the router that holds every router row in shared memory and gives each warp whole tokens;
+# 32 experts keep the cluster router: the same bits either way.
+@pytest.mark.parametrize("case", [(3, 512, None),                                # gpt-oss prefill, E=32
+                                  (5, 2048, None),                               # Mixtral prefill, E=8
+                                  (2, 100, dict(H=256, I=128, E=12, k=3)),       # E between classes
+                                  (1, 65, dict(H=160, I=64, E=5, k=2))],         # f16, 5 K steps of 32
+                         ids=_ids)
+def test_router_bit_exact_prefill_sizes(case):
+    test_router_bit_exact(case)
+
+
+def test_sigmoid_biased_router_prefill_size():
+    """The biased-sigmoid mode on the prefill-sized router: logits bit-exact, selection and
+    weights as the oracle's wherever the selection boundary is wider than the two sides' expf."""
+    moe = _moe()
+    L, D = _make(2, 300, dict(H=512, I=128, E=16, k=4))
+    c = dict(L["cfg"], mode="sigmoid_biased")
+    L = dict(L, cfg=c)
+    _, olg, oidx, ow = oracle_route(L, bits16(L["x"]))
+    idx, w, _, lg = moe.router_route(D["x"], D["Wr"], c["k"], mode="sigmoid_biased",
+                                     router_bias=D["router_bias"], want_logits=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(lg.cpu().numpy().view(np.uint32), olg.view(np.uint32))
+    keys = 1.0 / (1.0 + np.exp(-olg.astype(np.float64))) + L["router_bias"].cpu().numpy()
+    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+    checked = 0
+    for t in range(300):
+        srt = np.sort(keys[t])[::-1]
+        if np.min(np.abs(np.diff(srt[:c["k"] + 1]))) > 1e-6:
+            assert list(gi[t]) == list(oidx[t])
+            assert np.allclose(gw[t], ow[t], rtol=2e-6)
+            checked += 1
+    assert checked >= 250
+
+
 @pytest.mark.parametrize("T,E,k", [(1, 32, 4), (8, 128, 8), (512, 32, 4), (2048, 8, 2),
                                    (1500, 256, 16), (3, 5, 5),
                                    (131072, 64, 8)])          # a million routes: many chunks
