@@ -378,10 +378,10 @@ router_kernel(RouteArgs a, RouterPlan p) {
 // top-k.  Every logit has the fixed order of the cluster path above (lane l: fmaf over m
 // ascending, then the xor butterfly), so the two paths give the same bits; this one spends no
 // cluster barriers and loads the router rows once per SM instead of once per tile of a few
-// tokens.  Measured (one GB300): Mixtral T=2048 (E=8) router 43.8 -> 32.2 us; gpt-oss T=512
-// (E=32) 26.7 -> 34.3 us, where a warp's 32 partial sums per token cost more than the cluster
-// path's shared rows, so 32 experts keep that path.
-constexpr int kWideMaxWarps = 8;
+// tokens.  Measured (one GB300): Mixtral T=2048 (E=8) router 43.8 -> 24.7 us (8 warps per CTA:
+// 32.2); gpt-oss T=512 (E=32) 26.7 -> 34.3 us, where a warp's 32 partial sums per token cost
+// more than the cluster path's shared rows, so 32 experts keep that path.
+constexpr int kWideMaxWarps = 16;
 constexpr size_t kWideSmem = 227 * 1024;      // shared memory of one CTA
 constexpr int kWideMaxV = 16;                 // 16-byte pieces of a token row per lane (H <= 4096)
 constexpr uint32_t kWidePiece = 32 * 1024;    // bytes per bulk copy of the router rows
@@ -417,19 +417,22 @@ __global__ void __launch_bounds__(kWideMaxWarps * 32, 1) router_wide_kernel(Rout
     for (int t = blockIdx.x * nw + warp; t < a.T; t += gridDim.x * nw) {
         // the token row into this warp's buffer
         const uint4* src = reinterpret_cast<const uint4*>(xg + static_cast<size_t>(t) * H);
-        uint4 v[kWideMaxV];
 #pragma unroll
-        for (int q = 0; q < kWideMaxV; ++q)
-            if (lane + 32 * q < nv) v[q] = __ldg(src + lane + 32 * q);
+        for (int h = 0; h < kWideMaxV; h += 8) {          // two rounds of 8 loads in flight
+            uint4 v[8];
 #pragma unroll
-        for (int q = 0; q < kWideMaxV; ++q)
-            if (lane + 32 * q < nv) reinterpret_cast<uint4*>(xb)[lane + 32 * q] = v[q];
+            for (int q = 0; q < 8; ++q)
+                if (lane + 32 * (h + q) < nv) v[q] = __ldg(src + lane + 32 * (h + q));
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (lane + 32 * (h + q) < nv) reinterpret_cast<uint4*>(xb)[lane + 32 * (h + q)] = v[q];
+        }
         __syncwarp();
         float acc[EC];
 #pragma unroll
         for (int e = 0; e < EC; ++e) acc[e] = 0.0f;
         if (ok) {
-#pragma unroll 2
+#pragma unroll 4
             for (int j = lane; j < H; j += 32) {
                 const float xv = adt_bits_to_float(xb[j], a.adt);
 #pragma unroll
