@@ -371,35 +371,39 @@ router_kernel(RouteArgs a, RouterPlan p) {
     if (p.cl > 1) cluster_sync_all();
 }
 
-// Router for prefill-sized calls with few experts (no RMSNorm, at most 16 experts, router rows
-// that fit in shared memory): every CTA holds all E router rows (one bulk copy, split in pieces), each warp takes
-// whole tokens: it copies the token's row into its shared-memory buffer (16-byte loads, all
-// issued at once), then lane l keeps E partial sums over x[t][l + 32 m] and runs the token's
-// top-k.  Every logit has the fixed order of the cluster path above (lane l: fmaf over m
-// ascending, then the xor butterfly), so the two paths give the same bits; this one spends no
-// cluster barriers and loads the router rows once per SM instead of once per tile of a few
-// tokens.  Measured (one GB300): Mixtral T=2048 (E=8) router 43.8 -> 24.7 us (8 warps per CTA:
-// 32.2); gpt-oss T=512 (E=32) 26.7 -> 34.3 us, where a warp's 32 partial sums per token cost
-// more than the cluster path's shared rows, so 32 experts keep that path.
+// Router for prefill-sized calls (no RMSNorm, at most 32 experts, router rows that fit in shared
+// memory): every CTA holds all E router rows (one bulk copy, split in pieces) and takes rounds of
+// `tpc` tokens.  A token's row is copied into a shared-memory buffer (16-byte loads, all issued
+// at once) by the EG warps that share it; warp g of them keeps the partial sums of experts
+// 8 g .. 8 g + 7 over x[t][l + 32 m] (lane l), so every logit has the fixed order of the cluster
+// path above (lane l: fmaf over m ascending, then the xor butterfly) and the two paths give the
+// same bits; then one warp per token runs the top-k.  No cluster barriers, and the router rows
+// are loaded once per SM instead of once per tile of a few tokens.  Measured (one GB300, router
+// launch against the cluster path): Mixtral T=2048 (E=8) 43.8 -> 24.4 us, gpt-oss T=512 (E=32,
+// four warps per token) 26.1 -> 21.8 us.
 constexpr int kWideMaxWarps = 16;
 constexpr size_t kWideSmem = 227 * 1024;      // shared memory of one CTA
 constexpr int kWideMaxV = 16;                 // 16-byte pieces of a token row per lane (H <= 4096)
 constexpr uint32_t kWidePiece = 32 * 1024;    // bytes per bulk copy of the router rows
 
-template <int EC>   // expert count class: E <= EC
+template <int EG>   // warps per token: experts in groups of 8, E <= 8 EG
 __global__ void __launch_bounds__(kWideMaxWarps * 32, 1) router_wide_kernel(RouteArgs a) {
     extern __shared__ __align__(128) unsigned char rsm[];
     __shared__ __align__(8) uint64_t wfull;
     pdl_wait();                 // x may come from the previous kernel
     pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tpc = (blockDim.x >> 5) / EG;                     // token slots per round
+    const int ts = warp / EG, g = warp - ts * EG;               // this warp's slot and expert group
     const int E = a.E, H = a.H;
     const uint32_t wbytes = static_cast<uint32_t>(E) * H * 2;
     const size_t wal = (wbytes + 127) & ~127u;
-    const uint16_t* ws = reinterpret_cast<const uint16_t*>(rsm);                        // [E][H]
-    uint16_t* xb = reinterpret_cast<uint16_t*>(rsm + wal) + static_cast<size_t>(warp) * H;   // [nw][H]
-    float* scr = reinterpret_cast<float*>(rsm + wal + static_cast<size_t>(nw) * H * 2) +
-                 static_cast<size_t>(warp) * 4 * E;
+    const uint16_t* ws = reinterpret_cast<const uint16_t*>(rsm);                       // [E][H]
+    uint16_t* xb = reinterpret_cast<uint16_t*>(rsm + wal) + static_cast<size_t>(ts) * H;    // [tpc][H]
+    float* lg = reinterpret_cast<float*>(rsm + wal + static_cast<size_t>(tpc) * H * 2) +
+                static_cast<size_t>(ts) * E;                                            // [tpc][E]
+    float* scr = reinterpret_cast<float*>(rsm + wal + static_cast<size_t>(tpc) * H * 2) +
+                 static_cast<size_t>(tpc) * E + static_cast<size_t>(ts) * 4 * E;      // [tpc][4E]
     if (threadIdx.x == 0) {
         mbar_init(&wfull, 1);
         fence_mbar_init();
@@ -414,43 +418,57 @@ __global__ void __launch_bounds__(kWideMaxWarps * 32, 1) router_wide_kernel(Rout
     const bool ok = mbar_wait_bounded(&wfull, 0);
     const uint16_t* xg = static_cast<const uint16_t*>(a.x);
     const int nv = H / 8;
-    for (int t = blockIdx.x * nw + warp; t < a.T; t += gridDim.x * nw) {
-        // the token row into this warp's buffer
-        const uint4* src = reinterpret_cast<const uint4*>(xg + static_cast<size_t>(t) * H);
+    for (int base = blockIdx.x * tpc; base < a.T; base += gridDim.x * tpc) {
+        const int t = base + ts;
+        const bool have = t < a.T;
+        if (have) {
+            // the token row into its buffer: the slot's EG warps take its 16-byte pieces in turn
+            const uint4* src = reinterpret_cast<const uint4*>(xg + static_cast<size_t>(t) * H);
 #pragma unroll
-        for (int h = 0; h < kWideMaxV; h += 8) {          // two rounds of 8 loads in flight
-            uint4 v[8];
+            for (int h = 0; h < kWideMaxV / EG; h += 8) {
+                uint4 v[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (lane + 32 * (h + q) < nv) v[q] = __ldg(src + lane + 32 * (h + q));
+                for (int q = 0; q < 8; ++q) {
+                    const int pc = lane + 32 * (g + EG * (h + q));
+                    if (pc < nv) v[q] = __ldg(src + pc);
+                }
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (lane + 32 * (h + q) < nv) reinterpret_cast<uint4*>(xb)[lane + 32 * (h + q)] = v[q];
+                for (int q = 0; q < 8; ++q) {
+                    const int pc = lane + 32 * (g + EG * (h + q));
+                    if (pc < nv) reinterpret_cast<uint4*>(xb)[pc] = v[q];
+                }
+            }
         }
-        __syncwarp();
-        float acc[EC];
+        // rows in (and the last round's top-k done with lg and scr); one warp per token needs
+        // no more than its own barrier
+        if (EG > 1) __syncthreads(); else __syncwarp();
+        if (have) {
+            float acc[8];
 #pragma unroll
-        for (int e = 0; e < EC; ++e) acc[e] = 0.0f;
-        if (ok) {
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            const int e0 = 8 * g;
+            if (ok) {
 #pragma unroll 4
-            for (int j = lane; j < H; j += 32) {
-                const float xv = adt_bits_to_float(xb[j], a.adt);
+                for (int j = lane; j < H; j += 32) {
+                    const float xv = adt_bits_to_float(xb[j], a.adt);
 #pragma unroll
-                for (int e = 0; e < EC; ++e)
-                    if (e < E) acc[e] = __fmaf_rn(xv, adt_bits_to_float(ws[static_cast<size_t>(e) * H + j], a.adt), acc[e]);
+                    for (int i = 0; i < 8; ++i)
+                        if (e0 + i < E)
+                            acc[i] = __fmaf_rn(xv, adt_bits_to_float(ws[static_cast<size_t>(e0 + i) * H + j], a.adt), acc[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (e0 + i < E) {
+                    const float l = warp_sum_xor(acc[i]);
+                    if (lane == i) lg[e0 + i] = l;
+                }
             }
         }
-        float mine = 0.0f;                      // lane e: logit e
-#pragma unroll
-        for (int e = 0; e < EC; ++e) {
-            if (e < E) {
-                const float l = warp_sum_xor(acc[e]);
-                if (lane == e) mine = l;
-            }
-        }
-        route_token_warp([&](int) { return mine; }, bias_r, E, a.k, a.mode, a.bias != nullptr, a.scale, scr, t,
-                         a.idx, a.w, a.logits_out, !ok, lane);
-        __syncwarp();                           // the buffer and scr are the next token's
+        if (EG > 1) __syncthreads(); else __syncwarp();    // the token's logits in
+        if (have && g == 0)
+            route_token_warp([&](int e) { return lg[e]; }, bias_r, E, a.k, a.mode, a.bias != nullptr, a.scale, scr,
+                             t, a.idx, a.w, a.logits_out, !ok, lane);
     }
     // no copy may still be in flight when the CTA exits
     if (!ok && threadIdx.x == 0) mbar_wait_bounded(&wfull, 0);
@@ -536,23 +554,25 @@ build_routes_kernel(const int32_t* __restrict__ idx, int n, int E, int32_t* __re
 
 cudaError_t launch_router(const RouteArgs& a, cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
-    // prefill sizes: the router rows held in shared memory, whole tokens per warp
+    // prefill sizes: the router rows held in shared memory, rounds of whole tokens per CTA
+    const int EG = (a.E + 7) / 8;
     const size_t wal = (static_cast<size_t>(a.E) * a.H * 2 + 127) & ~size_t(127);
-    const size_t per_warp = static_cast<size_t>(a.H) * 2 + static_cast<size_t>(4) * a.E * 4;
-    const int nw = wal + per_warp <= kWideSmem
-                       ? static_cast<int>(std::min<size_t>(kWideMaxWarps, (kWideSmem - wal) / per_warp)) : 0;
-    if (a.x && !a.rmsnorm && !a.mxd_xs && a.T > 64 && a.E <= 16 && a.H % 8 == 0 && a.H <= 8 * 32 * kWideMaxV &&
-        nw >= 4 && (reinterpret_cast<uintptr_t>(a.Wr) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0) {
+    const size_t per_slot = static_cast<size_t>(a.H) * 2 + static_cast<size_t>(5) * a.E * 4;
+    const int tpc = wal + per_slot <= kWideSmem
+                        ? static_cast<int>(std::min<size_t>(kWideMaxWarps / EG, (kWideSmem - wal) / per_slot)) : 0;
+    if (a.x && !a.rmsnorm && !a.mxd_xs && a.T > 64 && a.E <= 32 && a.H % 8 == 0 && a.H <= 8 * 32 * kWideMaxV &&
+        tpc >= 2 && (reinterpret_cast<uintptr_t>(a.Wr) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15) == 0) {
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        const size_t smem = wal + static_cast<size_t>(nw) * per_warp;
-        const int grid = std::min(sms, (a.T + nw - 1) / nw);
-        auto kern = a.E <= 8 ? router_wide_kernel<8> : router_wide_kernel<16>;
+        const size_t smem = wal + static_cast<size_t>(tpc) * per_slot;
+        const int grid = std::min(sms, (a.T + tpc - 1) / tpc);
+        auto kern = EG == 1 ? router_wide_kernel<1> : EG == 2 ? router_wide_kernel<2>
+                  : EG == 3 ? router_wide_kernel<3> : router_wide_kernel<4>;
         e = ensure_smem(kern, smem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(kern, dim3(grid), dim3(nw * 32), smem, s, a);
+        return launch_pdl(kern, dim3(grid), dim3(tpc * EG * 32), smem, s, a);
     }
     const RouterPlan p = router_plan(a.T, a.H, a.E, a.x != nullptr);
     auto kern = a.mxd_xs ? router_kernel<true> : router_kernel<false>;

@@ -87,9 +87,9 @@ def test_router_bit_exact(case):
     assert np.array_equal(w2.cpu().numpy().view(np.uint32), w.cpu().numpy().view(np.uint32))
 
 
-# Prefill-sized router calls with few experts (more than 64 tokens, at most 16 experts, no RMSNorm)
-# take the router that holds every router row in shared memory and gives each warp whole tokens;
-# 32 experts keep the cluster router: the same bits either way.
+# Prefill-sized router calls (more than 64 tokens, at most 32 experts, no RMSNorm) take the router
+# that holds every router row in shared memory, each token's experts split over up to four warps:
+# the same bits as the cluster router.
 @pytest.mark.parametrize("case", [(3, 512, None),                                # gpt-oss prefill, E=32
                                   (5, 2048, None),                               # Mixtral prefill, E=8
                                   (2, 100, dict(H=256, I=128, E=12, k=3)),       # E between classes
