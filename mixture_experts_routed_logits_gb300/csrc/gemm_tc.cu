@@ -648,7 +648,7 @@ static TcLayout tc_layout(const GemmArgs& a, int num_sms, size_t* smem) {
     // MXFP4 calls take 128-route tiles: the epilogue of one item then overlaps the next item's
     // MMAs (two accumulator sets), which outweighs re-dequantising the weights of experts with
     // more than 128 routes
-    L.bn = Tk <= 256 ? 64 : (a.quant ? 128 : 256);
+    L.bn = Tk <= 256 ? 64 : (a.quant ? 128 : kBN);
     // shared-memory tail (barriers and the item tables) plus 1 KB for aligning the base to 1024
     constexpr size_t kTailBytes = (sizeof(SmemTail) + 255) / 256 * 256;
     const size_t tail = kTailBytes + 1024;
