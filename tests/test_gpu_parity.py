@@ -93,7 +93,11 @@ def test_router_bit_exact(case):
 @pytest.mark.parametrize("case", [(3, 512, None),                                # gpt-oss prefill, E=32
                                   (5, 2048, None),                               # Mixtral prefill, E=8
                                   (2, 100, dict(H=256, I=128, E=12, k=3)),       # E between classes
-                                  (1, 65, dict(H=160, I=64, E=5, k=2))],         # f16, 5 K steps of 32
+                                  (1, 65, dict(H=160, I=64, E=5, k=2)),          # f16, 5 K steps of 32
+                                  # the cluster router at prefill sizes: router rows past shared
+                                  # memory (32 x 4096 x 2 B), and more than 32 experts
+                                  (2, 65, dict(H=4096, I=128, E=32, k=4)),
+                                  (2, 70, dict(H=256, I=128, E=40, k=4))],
                          ids=_ids)
 def test_router_bit_exact_prefill_sizes(case):
     test_router_bit_exact(case)
